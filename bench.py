@@ -1,0 +1,430 @@
+"""Benchmark: one data-parallel-attention rank's MLA decode step on one GB300.
+
+A step is the whole hot path over one batch: for each of the workload's layers,
+append this step's new latent row of every sequence into that layer's paged
+cache, then decode every request over its full context (planned once per step,
+since all layers share the sequence lengths and block table).  Default
+workload: 20 sequences x 4096 tokens, 61 layers, 128 heads, page 64 (the
+rank's share of a 159 x 4096 node batch; 5.76 GB of cache read per step).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 3] [--impl reference]
+
+Prints one JSON line (rank 0).  `value` = cache bytes read per step / step
+time (GB/s), the throughput form of the step latency also reported as
+ms_per_step.  For N > 1 (torchrun) each rank runs an independent replica of
+the rank workload on its own GPU (no collective on the data path; a barrier
+and a max-reduction of the timings only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import mla_inputs as mi  # noqa: E402
+
+METRIC = "MLA decode step latency & cache GB/s at 1 GB300; % of roofline"
+ROW_BYTES = mi.ROW * 2
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workload
+
+def build_device_workload(w, device):
+    import torch
+    bt = mi.make_block_table(mi.rng_for(w.config_id, 0, 1), w.seq_lens, w.block_size,
+                             w.num_blocks())
+    layers = []
+    for l in range(w.layers):
+        d = mi.make_device_layer(w, l, device, block_table=bt)
+        layers.append(d)
+    shared = layers[0]
+    B = w.batch
+    outs = [torch.empty((B, 128, 512), dtype=torch.bfloat16, device=device) for _ in layers]
+    lses = [torch.empty((B, 128), dtype=torch.float32, device=device) for _ in layers]
+    return dict(layers=layers, bt=shared["block_table"], seq=shared["seq_lens"],
+                slots=shared["slot_mapping"], outs=outs, lses=lses, bt_host=bt)
+
+
+def algorithmic_bytes_per_layer(w):
+    cache = sum(w.seq_lens) * ROW_BYTES
+    q = w.batch * 128 * mi.ROW * 2
+    out = w.batch * 128 * 512 * 2
+    append = w.batch * ROW_BYTES if w.append else 0
+    return cache, q + out + cache, append
+
+
+def algorithmic_flops_per_layer(w):
+    return sum(w.seq_lens) * 2 * 128 * (mi.ROW + 512)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_mine(args, w, rank, world, local_rank):
+    import torch
+    import mla_latent_cache_decode_gb300 as mla
+
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    W = build_device_workload(w, device)
+    ws = mla.make_workspace(w.batch, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    # all work on one non-default stream (capturable into a CUDA graph)
+    stream = torch.cuda.Stream(device)
+    torch.cuda.set_stream(stream)
+    sh = stream.cuda_stream
+    L = w.layers
+    scale = mi.SOFTMAX_SCALE
+
+    def step(timing_events=None):
+        mla.mla_decode_plan(W["seq"], W["bt"], w.block_size, ws, dev_status=status, stream=sh)
+        for l in range(L):
+            d = W["layers"][l]
+            if w.append:
+                mla.mla_cache_append(d["kv_new"], W["slots"], d["cache"], dev_status=status,
+                                     stream=sh)
+            if timing_events is not None:
+                timing_events[l][0].record(stream)
+            mla.mla_decode_planned(d["q"], d["cache"], W["bt"], W["seq"], scale, W["outs"][l],
+                                   W["lses"][l], workspace=ws, dev_status=status, stream=sh)
+            if timing_events is not None:
+                timing_events[l][1].record(stream)
+
+    launches_per_step = 1 + L * ((1 if w.append else 0) + 2)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # ---- timed region: exactly K steps, device events on the launching stream
+    clocks = ClockSampler(local_rank)
+    if rank == 0:
+        clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop() if rank == 0 else None
+    ms_total = e0.elapsed_time(e1)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_total], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+
+    # ---- per-launch duration of the decode kernel (events around each launch)
+    kev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+           for _ in range(L)]
+    ksteps = max(1, min(args.steps, 20))
+    kms = []
+    for _ in range(ksteps):
+        step(kev)
+        torch.cuda.synchronize()
+        kms += [a.elapsed_time(b) for a, b in kev]
+    decode_ms = statistics.mean(kms)
+
+    # ---- e2e through the C ABI with host buffers (pinned), copies inside the timed region
+    q_host = [d["q"].cpu().pin_memory() for d in W["layers"]]
+    kv_host = [d["kv_new"].cpu().pin_memory() for d in W["layers"]]
+    seq_host = W["seq"].cpu().pin_memory()
+    bt_host = W["bt"].cpu().pin_memory()
+    slot_host = W["slots"].cpu().pin_memory()
+    out_host = [torch.empty_like(o, device="cpu").pin_memory() for o in W["outs"]]
+    qd = [torch.empty_like(d["q"]) for d in W["layers"]]
+    kvd = [torch.empty_like(d["kv_new"]) for d in W["layers"]]
+    seqd, btd, slotd = (torch.empty_like(W["seq"]), torch.empty_like(W["bt"]),
+                        torch.empty_like(W["slots"]))
+    h2d = sum(t.numel() * t.element_size() for t in q_host + kv_host + [seq_host, bt_host, slot_host])
+    d2h = sum(t.numel() * t.element_size() for t in out_host)
+
+    def e2e_step():
+        seqd.copy_(seq_host, non_blocking=True)
+        btd.copy_(bt_host, non_blocking=True)
+        slotd.copy_(slot_host, non_blocking=True)
+        mla.mla_decode_plan(seqd, btd, w.block_size, ws, dev_status=status, stream=sh)
+        for l in range(L):
+            d = W["layers"][l]
+            qd[l].copy_(q_host[l], non_blocking=True)
+            kvd[l].copy_(kv_host[l], non_blocking=True)
+            if w.append:
+                mla.mla_cache_append(kvd[l], slotd, d["cache"], dev_status=status, stream=sh)
+            mla.mla_decode_planned(qd[l], d["cache"], btd, seqd, scale, W["outs"][l],
+                                   W["lses"][l], workspace=ws, dev_status=status, stream=sh)
+            out_host[l].copy_(W["outs"][l], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    esteps = max(1, min(args.steps, 50))
+    barrier()
+    t0 = time.perf_counter()
+    a0 = torch.cuda.Event(enable_timing=True)
+    a1 = torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(esteps):
+        e2e_step()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max(a0.elapsed_time(a1), (time.perf_counter() - t0) * 1e3) / esteps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    assert int(status.item()) == 0
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return None
+
+    cache_b, decode_b, append_b = algorithmic_bytes_per_layer(w)
+    step_cache_bytes = cache_b * L
+    value = world * step_cache_bytes / (ms_step * 1e-3) / 1e9
+    hbm_peak, tf_peak, src = measured_peaks()
+    achieved = decode_b / (decode_ms * 1e-3) / 1e9
+    step_bytes = (decode_b + append_b) * L
+    roofline_step_us = max(step_bytes / (hbm_peak * 1e9),
+                           algorithmic_flops_per_layer(w) * L / (tf_peak * 1e12)) * 1e6
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "step_latency_us": round(ms_step * 1e3, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "seq_len": w.seq_lens[0]
+                   if len(set(w.seq_lens)) == 1 else "mixed", "layers": L, "heads": 128,
+                   "block_size": w.block_size, "cache_gb_per_step": round(step_cache_bytes / 1e9, 4),
+                   "l2": f"inputs larger than L2: {step_cache_bytes / 1e9:.2f} GB of cache per step"
+                   if step_cache_bytes > 256e6 else "L2 not flushed (small workload)",
+                   "cuda_graph": graph is not None,
+                   "parallelism": "dp-attention rank per GPU; replicas only"},
+        "step_roofline_frac": round(roofline_step_us / (ms_step * 1e3), 4),
+        "roofline": {"bound": "hbm", "kernel": "mla decode", "achieved": round(achieved, 1),
+                     "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                     "peak_source": src, "traffic": None,
+                     "algorithmic_bytes_per_launch": decode_b,
+                     "launch_us": round(decode_ms * 1e3, 2)},
+        "e2e": {"value": round(world * step_cache_bytes / (e2e_ms * 1e-3) / 1e9, 2),
+                "unit": "GB/s", "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, W, budget_s=args.cpu_budget)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return result
+
+
+# ----------------------------------------------------------------------------- oracle on the host
+
+def _host_layer_for_oracle(w, d, bt):
+    import oracle  # noqa: F401
+    return dict(q=mi.to_bits(d["q"]), cache=mi.to_bits(d["cache"]), bt=bt,
+                seq=d["seq_lens"].cpu().numpy(), kv=mi.to_bits(d["kv_new"]),
+                slots=d["slot_mapping"].cpu().numpy())
+
+
+def cpu_baseline(w, W, budget_s=15.0):
+    """The fp64 oracle, as it stands, on the host cores over a bounded sample."""
+    import oracle
+    done_bytes, t_used, layers_done = 0, 0.0, 0
+    for l in range(w.layers):
+        h = _host_layer_for_oracle(w, W["layers"][l], W["bt_host"])
+        t0 = time.perf_counter()
+        cache = h["cache"]
+        if w.append:
+            oracle.append(h["kv"], h["slots"], cache)
+        oracle.decode(h["q"], cache, h["bt"], h["seq"], mi.SOFTMAX_SCALE)
+        t_used += time.perf_counter() - t0
+        done_bytes += sum(w.seq_lens) * ROW_BYTES
+        layers_done += 1
+        if t_used >= budget_s:
+            break
+    return {"value": round(done_bytes / t_used / 1e9, 4), "unit": "GB/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{layers_done} of {w.layers} layers (append + decode of all {w.batch} "
+                      f"requests), {t_used:.1f} s"}
+
+
+def run_reference(args, w, rank, world):
+    """Reference arm: the oracle, timed on the host cores, on the same workload and metric."""
+    if rank != 0:
+        return None
+    import oracle
+    rng = mi.rng_for(w.config_id, 0, 1)
+    bt = mi.make_block_table(rng, w.seq_lens, w.block_size, w.num_blocks())
+    # one request of one layer per step: bounded so K + W steps finish in minutes
+    b = 0
+    L = w.seq_lens[b]
+    need = -(-L // w.block_size)
+    g = np.random.default_rng(mi.BASE_SEED + w.config_id)
+    cache = np.full((w.num_blocks(), w.block_size, mi.ROW), mi.BF16_NAN, np.uint16)
+    blocks = bt[b, :need]
+    cache[blocks] = mi.f32_to_bf16_bits(
+        g.standard_normal((need, w.block_size, mi.ROW), dtype=np.float32))
+    q = mi.make_queries(g, 1)
+    kv = mi.f32_to_bf16_bits(g.standard_normal((1, mi.ROW), dtype=np.float32))
+    slots = np.array([mi.slot_of(bt, b, L - 1, w.block_size)], np.int64)
+    seq = np.array([L], np.int32)
+
+    def step():
+        oracle.append(kv, slots, cache)
+        oracle.decode(q, cache, bt[b:b + 1], seq, mi.SOFTMAX_SCALE)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = L * ROW_BYTES / dt / 1e9
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "layers": w.layers,
+                       "heads": 128, "block_size": w.block_size,
+                       "parallelism": "dp-attention rank per GPU; replicas only"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s",
+                             "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": f"each step: append + decode of 1 of {w.batch} requests "
+                                       f"({L} tokens, 128 heads) of 1 of {w.layers} layers"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=3)
+    ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local_rank = dist_env()
+    w = mi.workload(args.config)
+    if args.impl == "reference":
+        res = run_reference(args, w, rank, world)
+    else:
+        res = run_mine(args, w, rank, world, local_rank)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,198 @@
+/*
+ * libmla — MLA latent-cache decode for one data-parallel-attention rank on a
+ * GB300 (sm_103a).  C ABI: plain pointers and sizes, no framework types.
+ *
+ * The operation (absorbed-form Multi-head Latent Attention decode):
+ *   Each cached token holds ONE 576-wide latent row shared by all heads:
+ *   elements 0..511 are kv_c (kv_lora_rank = 512) and 512..575 the MQA-style
+ *   k_rope (64 dims shared by every head), stored per layer as [NB, BS, 576]
+ *   [MLA 的 TP 切分：为什么 8 张 GPU 存了同一份 KV cache (10100.com), section 2.2
+ *   "三个事实" and section 3.1 (MLAAttentionSpec: num_kv_heads = 1,
+ *   head_size = 576; per-layer cache [NB, BS, 576])].
+ *   In decode the engine runs the absorbed form: every head's query is already
+ *   projected into the latent space (q_nope . W_UK -> 512 dims, plus 64 rope
+ *   dims) and attends over the shared latent directly
+ *   [dp-attention-expert-parallel-mla-kv-replication (inferenceinterviews.com),
+ *   "A strong answer"].  The value is the 512-dim kv_c itself
+ *   (v_head_dim = kv_lora_rank) [DP 与 DPA 的区别：SGLang 并行部署与路由
+ *   (chengxuchu.com), "MLA：KV 是一份共享 latent"].  For request b with context
+ *   length L and head h:
+ *       s_t  = softmax_scale * sum_{d<576} q[b,h,d] * row_t[d]
+ *       out[b,h,j] = sum_t softmax(s)_t * row_t[j]          (j < 512)
+ *       lse[b,h]   = log sum_t exp(s_t)                     (natural log)
+ *   where row_t = cache[block_table[b][t / BS]][t % BS].
+ *   With data-parallel attention a rank owns its requests, their cache and the
+ *   full attention weights, so this step needs no communication between GPUs
+ *   [dp-attention-expert-parallel-mla-kv-replication, "The fix"]; a rank with no
+ *   requests still runs the step with an empty batch ["What it costs"], which
+ *   here is batch = 0, a valid no-op.
+ *
+ * Conventions shared by every entry point
+ *   - Device pointers are CUDA device (or managed) memory of the current
+ *     device; host pointers are named *_host.  The caller owns every buffer.
+ *     The library allocates and frees nothing, never synchronises, and launches
+ *     only on the caller's stream (a cudaStream_t passed as void*; NULL = the
+ *     legacy default stream).
+ *   - Tensors are dense, row-major, with the shapes given.  bf16 = IEEE
+ *     bfloat16 stored as 16-bit values.  Device pointers to bf16/fp32 data
+ *     must be 16-byte aligned.
+ *   - Arguments are checked on the host before any launch; a failed check
+ *     returns a status and launches nothing.  mla_last_error_detail() then
+ *     describes it (thread-local string).
+ *   - Faults the host cannot see (a block-table entry or slot outside the
+ *     pool, a sequence longer than its table) are reported by the kernels into
+ *     *dev_status (optional, device int32, first error wins; 0 = none): the
+ *     kernels never trap.  Read it after synchronising the stream.  Results of
+ *     a request touched by such a fault are unspecified.
+ *   - Every bounded wait inside a kernel gives up after a fixed time budget
+ *     and reports MLA_ERR_DEVICE_TIMEOUT in *dev_status instead of hanging.
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_ABI_VERSION 1
+#define MLA_ROW_DIM 576       /* 512 kv_c + 64 k_rope per cached token */
+#define MLA_KV_LORA_RANK 512  /* value / output width */
+#define MLA_ROPE_DIM 64
+#define MLA_NUM_HEADS 128     /* heads per request the decode supports */
+
+typedef enum mla_status {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARGUMENT = 1,    /* host-side check failed, nothing launched */
+  MLA_ERR_UNSUPPORTED = 2,         /* valid but not supported (e.g. num_heads != 128) */
+  MLA_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < mla_decode_workspace_size() */
+  MLA_ERR_CUDA = 4,                /* a CUDA runtime call or launch failed */
+  MLA_ERR_DEVICE_RANGE = 5,        /* device-seen: bad block id, slot or length */
+  MLA_ERR_DEVICE_TIMEOUT = 6       /* device-seen: a bounded wait expired */
+} mla_status_t;
+
+/* Name of a status code ("MLA_OK", ...); never NULL. */
+const char *mla_status_string(int status);
+
+/* Detail of the last failed call on this host thread ("" if none). */
+const char *mla_last_error_detail(void);
+
+/* MLA_ABI_VERSION of the loaded library. */
+int mla_abi_version(void);
+
+/*
+ * mla_cache_append — store each new token's 576-wide latent row into its slot.
+ *
+ * Defined by: the per-token output of kv_a_proj_with_mqa is one 512 + 64 = 576
+ * wide row, replicated rather than split by head, and it is what the MLA cache
+ * stores [MLA 的 TP 切分 (10100.com), section 2.2 and 3.1].
+ *
+ *   kv_new        bf16 [num_tokens, 576]  rows to store (copied bit-exactly).
+ *   slot_mapping  int64 [num_tokens]      slot = block * block_size + row;
+ *                                         -1 = skip this token.
+ *   cache         bf16 [num_blocks, block_size, 576], updated in place.
+ * num_tokens = 0 is a no-op.  A slot outside [-1, num_blocks*block_size) is
+ * skipped and reported as MLA_ERR_DEVICE_RANGE in *dev_status.  Two tokens
+ * with the same slot race (either row may win).  block_size >= 1.
+ */
+mla_status_t mla_cache_append(const void *kv_new, const int64_t *slot_mapping,
+                              int64_t num_tokens, void *cache, int64_t num_blocks,
+                              int32_t block_size, int32_t *dev_status, void *stream);
+
+/*
+ * mla_decode_workspace_size — bytes of scratch mla_decode needs on the
+ * current device for `batch` requests of `num_heads` heads.  The workspace
+ * holds the split plan (units of the token partition, per request) and the
+ * fp32 partial results of requests that are split across CTAs.
+ */
+size_t mla_decode_workspace_size(int32_t batch, int32_t num_heads);
+
+/*
+ * mla_decode_plan — compute the split-KV plan for these sequence lengths
+ * into the workspace (one small kernel).  The plan depends only on seq_lens,
+ * batch, max_blocks_per_seq and block_size, so a caller decoding many layers
+ * of one step with the same lengths plans once and then calls
+ * mla_decode_planned per layer.  Lengths are read on the device; a length
+ * outside [0, max_blocks_per_seq * block_size] is clamped and reported as
+ * MLA_ERR_DEVICE_RANGE.
+ */
+mla_status_t mla_decode_plan(const int32_t *seq_lens, int32_t batch, int32_t num_heads,
+                             int32_t max_blocks_per_seq, int32_t block_size,
+                             void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                             void *stream);
+
+/*
+ * mla_decode — absorbed-form MLA decode (the equation at the top of this file).
+ * Runs mla_decode_plan and then mla_decode_planned.
+ *
+ *   q             bf16 [batch, num_heads, 576]  absorbed queries (512 latent
+ *                 dims from q_nope . W_UK, then 64 already-rotated rope dims).
+ *   cache         bf16 [num_blocks, block_size, 576] this layer's latent cache.
+ *   block_table   int32 [batch, max_blocks_per_seq]; entry i of request b is
+ *                 the physical block of tokens [i*BS, (i+1)*BS).  Only the
+ *                 first ceil(seq_lens[b] / BS) entries are read.
+ *   seq_lens      int32 [batch] (device) context lengths; 0 gives out = 0 and
+ *                 lse = -inf for that request.
+ *   max_seq_len   host upper bound of seq_lens (checked against the table).
+ *   softmax_scale multiplies q . row (e.g. 1/sqrt(192) for 128 + 64 dim heads).
+ *   out           bf16 [batch, num_heads, 512] (written).
+ *   lse           fp32 [batch, num_heads] natural-log sum-exp, or NULL.
+ *   workspace     device scratch of >= mla_decode_workspace_size(batch,
+ *                 num_heads) bytes, 256-byte aligned, zero-filled before its
+ *                 first use.  Calls leave it ready for the next call; calls
+ *                 sharing one workspace must not overlap on the GPU.
+ * Requirements: num_heads == 128; block_size in {16, 32, 64, 128, 256};
+ * max_seq_len <= max_blocks_per_seq * block_size; batch >= 0 (0 = no-op).
+ * Rows the plan does not cover (tails past seq_len, unused blocks) are never
+ * read, whatever they hold.
+ */
+mla_status_t mla_decode(const void *q, const void *cache, int64_t num_blocks, int32_t block_size,
+                        const int32_t *block_table, int32_t max_blocks_per_seq,
+                        const int32_t *seq_lens, int32_t batch, int32_t num_heads,
+                        int32_t max_seq_len, float softmax_scale, void *out, float *lse,
+                        void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                        void *stream);
+
+/*
+ * mla_decode_planned — mla_decode using the plan already in `workspace`
+ * (from mla_decode_plan with the same seq_lens, batch, block_size and
+ * max_blocks_per_seq).  Same arguments and results as mla_decode.
+ */
+mla_status_t mla_decode_planned(const void *q, const void *cache, int64_t num_blocks,
+                                int32_t block_size, const int32_t *block_table,
+                                int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                int32_t batch, int32_t num_heads, int32_t max_seq_len,
+                                float softmax_scale, void *out, float *lse, void *workspace,
+                                size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
+ * mla_combine — merge split-KV partial results (flash-decoding).
+ *
+ * Partial w (one token range of one request) holds o_partial[w] = its own
+ * normalised output and lse_partial[w] = log-sum-exp of its scores.  Request
+ * b owns partials [split_offsets[b], split_offsets[b+1]) and gets
+ *   M = max_w lse_w,  a_w = exp(lse_w - M),
+ *   out[b,h,:] = sum_w a_w o_w[h,:] / sum_w a_w,   lse[b,h] = M + log sum_w a_w.
+ * A partial with lse = -inf (an empty range) has no weight; a request with no
+ * weighted partial gets out = 0, lse = -inf.  This regrouping of one softmax
+ * over disjoint ranges is standard split-KV decoding, not on the pages; it is
+ * how a long request is spread over many CTAs so it does not stall the batch
+ * [dp-attention-expert-parallel-mla-kv-replication, "What it costs": a rank
+ * holding long-context requests runs slower attention while others wait].
+ *
+ *   o_partial     fp32 [W, num_heads, 512];  lse_partial fp32 [W, num_heads]
+ *   split_offsets int32 [batch + 1] (device), non-decreasing, last = W.
+ *   out           bf16 [batch, num_heads, 512];  lse fp32 [batch, num_heads] or NULL.
+ * Any num_heads >= 1.
+ */
+mla_status_t mla_combine(const float *o_partial, const float *lse_partial,
+                         const int32_t *split_offsets, int32_t batch, int32_t num_heads,
+                         void *out, float *lse, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

@@ -1,0 +1,210 @@
+"""Python binding of libmla (MLA latent-cache decode on GB300 / sm_103a).
+
+Argument marshalling only: each function below checks dtypes/shapes of the
+PyTorch tensors it is given, passes raw device pointers, sizes and the current
+CUDA stream to the C ABI declared in include/mla.h, and raises MlaError on a
+non-zero status.  Every step of the computation runs in the library's CUDA
+kernels; there is no other implementation to fall back to: the first call
+raises ImportError if the compiled library is missing.
+
+Functions carry the C names: mla_cache_append, mla_decode_plan, mla_decode,
+mla_decode_planned, mla_combine, mla_decode_workspace_size.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libmla.so")
+
+ROW_DIM = 576
+KV_LORA_RANK = 512
+ROPE_DIM = 64
+NUM_HEADS = 128
+
+STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARGUMENT", 2: "MLA_ERR_UNSUPPORTED",
+          3: "MLA_ERR_WORKSPACE_TOO_SMALL", 4: "MLA_ERR_CUDA", 5: "MLA_ERR_DEVICE_RANGE",
+          6: "MLA_ERR_DEVICE_TIMEOUT"}
+EXPORTED = ("mla_status_string", "mla_last_error_detail", "mla_abi_version", "mla_cache_append",
+            "mla_decode_workspace_size", "mla_decode_plan", "mla_decode", "mla_decode_planned",
+            "mla_combine")
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        super().__init__(f"{STATUS.get(status, status)}: {detail}")
+        self.status = status
+        self.detail = detail
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libmla is not built ({LIB_PATH} missing): run "
+                          "`python -m mla_latent_cache_decode_gb300.build` first")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                            ctypes.c_size_t)
+    lib.mla_status_string.argtypes = [ctypes.c_int]
+    lib.mla_status_string.restype = ctypes.c_char_p
+    lib.mla_last_error_detail.argtypes = []
+    lib.mla_last_error_detail.restype = ctypes.c_char_p
+    lib.mla_abi_version.argtypes = []
+    lib.mla_abi_version.restype = ctypes.c_int
+    lib.mla_cache_append.argtypes = [P, P, i64, P, i64, i32, P, P]
+    lib.mla_cache_append.restype = ctypes.c_int
+    lib.mla_decode_workspace_size.argtypes = [i32, i32]
+    lib.mla_decode_workspace_size.restype = sz
+    lib.mla_decode_plan.argtypes = [P, i32, i32, i32, i32, P, sz, P, P]
+    lib.mla_decode_plan.restype = ctypes.c_int
+    dec = [P, P, i64, i32, P, i32, P, i32, i32, i32, f32, P, P, P, sz, P, P]
+    lib.mla_decode.argtypes = dec
+    lib.mla_decode.restype = ctypes.c_int
+    lib.mla_decode_planned.argtypes = dec
+    lib.mla_decode_planned.restype = ctypes.c_int
+    lib.mla_combine.argtypes = [P, P, P, i32, i32, P, P, P]
+    lib.mla_combine.restype = ctypes.c_int
+    return lib
+
+
+_lib = None
+
+
+def get_lib():
+    """The loaded libmla (loaded on first use; raises ImportError if not built)."""
+    global _lib
+    if _lib is None:
+        _lib = _load()
+    return _lib
+
+
+def __getattr__(name):
+    if name == "lib":
+        return get_lib()
+    raise AttributeError(name)
+
+
+def _check(status: int):
+    if status != 0:
+        raise MlaError(status, get_lib().mla_last_error_detail().decode())
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _need(t, dtype, ndim, name):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype or t.dim() != ndim or not t.is_contiguous() or not t.is_cuda:
+        raise ValueError(f"{name}: need contiguous CUDA {dtype} with {ndim} dims, got "
+                         f"{t.dtype} {tuple(t.shape)} on {t.device}")
+
+
+def mla_decode_workspace_size(batch: int, num_heads: int = NUM_HEADS) -> int:
+    return int(get_lib().mla_decode_workspace_size(batch, num_heads))
+
+
+def make_workspace(batch: int, num_heads: int = NUM_HEADS, device=None):
+    """A workspace tensor of the size mla_decode needs on the current device."""
+    import torch
+    n = mla_decode_workspace_size(batch, num_heads)
+    if n == 0:
+        raise MlaError(4, "cannot size the workspace (no CUDA device?)")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def mla_cache_append(kv_new, slot_mapping, cache, dev_status=None, stream=None):
+    """cache[slot // BS, slot % BS, :] = kv_new[i] for every slot != -1 (bit-exact)."""
+    import torch
+    _need(kv_new, torch.bfloat16, 2, "kv_new")
+    _need(slot_mapping, torch.int64, 1, "slot_mapping")
+    _need(cache, torch.bfloat16, 3, "cache")
+    if kv_new.shape[1] != ROW_DIM or cache.shape[2] != ROW_DIM:
+        raise ValueError("rows must be 576 wide")
+    if slot_mapping.shape[0] != kv_new.shape[0]:
+        raise ValueError("slot_mapping and kv_new disagree on the token count")
+    _check(get_lib().mla_cache_append(_ptr(kv_new), _ptr(slot_mapping), kv_new.shape[0], _ptr(cache),
+                                cache.shape[0], cache.shape[1], _ptr(dev_status),
+                                _stream(stream)))
+
+
+def mla_decode_plan(seq_lens, block_table, block_size, workspace, num_heads=NUM_HEADS,
+                    dev_status=None, stream=None):
+    import torch
+    _need(seq_lens, torch.int32, 1, "seq_lens")
+    _need(block_table, torch.int32, 2, "block_table")
+    _check(get_lib().mla_decode_plan(_ptr(seq_lens), seq_lens.shape[0], num_heads,
+                               block_table.shape[1], block_size, _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _ptr(dev_status),
+                               _stream(stream)))
+
+
+def _decode(fn, q, cache, block_table, seq_lens, softmax_scale, out, lse, workspace,
+            max_seq_len, dev_status, stream):
+    import torch
+    _need(q, torch.bfloat16, 3, "q")
+    _need(cache, torch.bfloat16, 3, "cache")
+    _need(block_table, torch.int32, 2, "block_table")
+    _need(seq_lens, torch.int32, 1, "seq_lens")
+    _need(out, torch.bfloat16, 3, "out")
+    if lse is not None:
+        _need(lse, torch.float32, 2, "lse")
+    B, H, row = q.shape
+    if row != ROW_DIM or cache.shape[2] != ROW_DIM or tuple(out.shape) != (B, H, KV_LORA_RANK):
+        raise ValueError("shape mismatch: q [B,H,576], cache [NB,BS,576], out [B,H,512]")
+    if seq_lens.shape[0] != B or block_table.shape[0] != B:
+        raise ValueError("seq_lens / block_table batch mismatch")
+    if max_seq_len is None:
+        max_seq_len = block_table.shape[1] * cache.shape[1]
+    _check(fn(_ptr(q), _ptr(cache), cache.shape[0], cache.shape[1], _ptr(block_table),
+              block_table.shape[1], _ptr(seq_lens), B, H, int(max_seq_len), float(softmax_scale),
+              _ptr(out), _ptr(lse), _ptr(workspace),
+              workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream)))
+    return out
+
+
+def mla_decode(q, cache, block_table, seq_lens, softmax_scale, out, lse=None, workspace=None,
+               max_seq_len=None, dev_status=None, stream=None):
+    """Absorbed-form MLA decode: out[b,h] = softmax(scale * q[b,h] . rows) @ rows[:, :512]."""
+    if workspace is None:
+        workspace = make_workspace(q.shape[0], q.shape[1], q.device)
+    return _decode(get_lib().mla_decode, q, cache, block_table, seq_lens, softmax_scale, out, lse,
+                   workspace, max_seq_len, dev_status, stream)
+
+
+def mla_decode_planned(q, cache, block_table, seq_lens, softmax_scale, out, lse=None,
+                       workspace=None, max_seq_len=None, dev_status=None, stream=None):
+    """mla_decode reusing the plan mla_decode_plan wrote into `workspace`."""
+    return _decode(get_lib().mla_decode_planned, q, cache, block_table, seq_lens, softmax_scale, out,
+                   lse, workspace, max_seq_len, dev_status, stream)
+
+
+def mla_combine(o_partial, lse_partial, split_offsets, out, lse=None, stream=None):
+    """Log-sum-exp merge of split partials (fp32 [W,H,512], [W,H]) into out bf16 [B,H,512]."""
+    import torch
+    _need(o_partial, torch.float32, 3, "o_partial")
+    _need(lse_partial, torch.float32, 2, "lse_partial")
+    _need(split_offsets, torch.int32, 1, "split_offsets")
+    _need(out, torch.bfloat16, 3, "out")
+    B = split_offsets.shape[0] - 1
+    H = o_partial.shape[1]
+    if o_partial.shape[2] != KV_LORA_RANK or tuple(out.shape) != (B, H, KV_LORA_RANK):
+        raise ValueError("shape mismatch")
+    _check(get_lib().mla_combine(_ptr(o_partial), _ptr(lse_partial), _ptr(split_offsets), B, H,
+                           _ptr(out), _ptr(lse), _stream(stream)))
+    return out

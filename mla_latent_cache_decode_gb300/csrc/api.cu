@@ -1,0 +1,237 @@
+// C-ABI entry points of libmla: argument checks, workspace sizing, launches.
+// Every public function validates on the host before launching anything and
+// returns an mla_status_t; details of a failure go to a thread-local string.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+
+namespace mla {
+cudaError_t launch_cache_append(const void *kv_new, const int64_t *slots, int64_t num_tokens,
+                                void *cache, int64_t num_slots, int32_t *dev_status,
+                                cudaStream_t stream);
+cudaError_t launch_plan(const int32_t *seq_lens, int32_t batch, int32_t unit_tokens,
+                        int32_t max_blocks_per_seq, int32_t block_size, int32_t max_ranges,
+                        void *ws, int32_t heads, int32_t *dev_status, cudaStream_t stream);
+cudaError_t launch_plan_combine(void *ws, int32_t batch, int32_t heads, int32_t max_ranges,
+                                void *out, float *lse, cudaStream_t stream);
+cudaError_t launch_offsets_combine(const float *o_part, const float *lse_part,
+                                   const int32_t *offsets, int32_t batch, int32_t heads, void *out,
+                                   float *lse, cudaStream_t stream);
+int simt_unit_tokens();
+cudaError_t launch_decode_simt(const void *q, const void *cache, int64_t num_blocks,
+                               int32_t block_size, const int32_t *block_table,
+                               int32_t max_blocks_per_seq, int32_t batch, float softmax_scale,
+                               void *out, float *lse, void *ws, int32_t max_ranges,
+                               int32_t *dev_status, cudaStream_t stream);
+
+namespace {
+
+thread_local std::string g_detail;
+
+mla_status_t fail(mla_status_t s, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_detail = buf;
+  return s;
+}
+
+mla_status_t cuda_fail(cudaError_t e, const char *what) {
+  return fail(MLA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Per-device SM count, cached (the only host state besides g_detail).
+int sm_count_current(int *out_dev) {
+  static std::mutex mu;
+  static int counts[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  if (out_dev) *out_dev = dev;
+  std::lock_guard<std::mutex> lock(mu);
+  if (counts[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    counts[dev] = n;
+  }
+  return counts[dev];
+}
+
+// Ranges of the plan: one per SM.
+int max_ranges_current() { return sm_count_current(nullptr); }
+
+bool block_size_ok(int32_t bs) { return bs == 16 || bs == 32 || bs == 64 || bs == 128 || bs == 256; }
+
+mla_status_t check_decode_args(const void *q, const void *cache, int64_t num_blocks,
+                               int32_t block_size, const int32_t *block_table,
+                               int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t batch,
+                               int32_t num_heads, int32_t max_seq_len, float softmax_scale,
+                               void *out, float *lse, void *workspace, size_t workspace_bytes) {
+  if (batch < 0) return fail(MLA_ERR_INVALID_ARGUMENT, "batch %d < 0", batch);
+  if (num_heads != kHeads)
+    return fail(MLA_ERR_UNSUPPORTED, "num_heads %d: only %d is supported", num_heads, kHeads);
+  if (block_size <= 0) return fail(MLA_ERR_INVALID_ARGUMENT, "block_size %d <= 0", block_size);
+  if (!block_size_ok(block_size))
+    return fail(MLA_ERR_UNSUPPORTED, "block_size %d not in {16,32,64,128,256}", block_size);
+  if (batch == 0) return MLA_OK;
+  if (!q || !cache || !block_table || !seq_lens || !out || !workspace)
+    return fail(MLA_ERR_INVALID_ARGUMENT, "null pointer argument");
+  if (!aligned(q, 16) || !aligned(cache, 16) || !aligned(out, 16))
+    return fail(MLA_ERR_INVALID_ARGUMENT, "q, cache and out must be 16-byte aligned");
+  if (!aligned(block_table, 4) || !aligned(seq_lens, 4) || (lse && !aligned(lse, 4)))
+    return fail(MLA_ERR_INVALID_ARGUMENT, "block_table, seq_lens, lse must be 4-byte aligned");
+  if (!aligned(workspace, 256))
+    return fail(MLA_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
+  if (num_blocks <= 0 || num_blocks > (int64_t)INT32_MAX)
+    return fail(MLA_ERR_INVALID_ARGUMENT, "num_blocks %lld out of range", (long long)num_blocks);
+  if (max_blocks_per_seq <= 0)
+    return fail(MLA_ERR_INVALID_ARGUMENT, "max_blocks_per_seq %d <= 0", max_blocks_per_seq);
+  if ((int64_t)max_blocks_per_seq * block_size > (int64_t)INT32_MAX / 2)
+    return fail(MLA_ERR_INVALID_ARGUMENT, "max_blocks_per_seq * block_size too large");
+  if (max_seq_len < 0 || (int64_t)max_seq_len > (int64_t)max_blocks_per_seq * block_size)
+    return fail(MLA_ERR_INVALID_ARGUMENT, "max_seq_len %d outside [0, %lld]", max_seq_len,
+                (long long)max_blocks_per_seq * block_size);
+  if (!std::isfinite(softmax_scale))
+    return fail(MLA_ERR_INVALID_ARGUMENT, "softmax_scale is not finite");
+  const size_t need = mla_decode_workspace_size(batch, num_heads);
+  if (need == 0) return fail(MLA_ERR_CUDA, "cannot query the current device");
+  if (workspace_bytes < need)
+    return fail(MLA_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed", workspace_bytes,
+                need);
+  return MLA_OK;
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+const char *mla_status_string(int status) {
+  switch (status) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARGUMENT: return "MLA_ERR_INVALID_ARGUMENT";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_WORKSPACE_TOO_SMALL: return "MLA_ERR_WORKSPACE_TOO_SMALL";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_DEVICE_RANGE: return "MLA_ERR_DEVICE_RANGE";
+    case MLA_ERR_DEVICE_TIMEOUT: return "MLA_ERR_DEVICE_TIMEOUT";
+    default: return "MLA_ERR_UNKNOWN";
+  }
+}
+
+const char *mla_last_error_detail(void) { return g_detail.c_str(); }
+
+int mla_abi_version(void) { return MLA_ABI_VERSION; }
+
+mla_status_t mla_cache_append(const void *kv_new, const int64_t *slot_mapping, int64_t num_tokens,
+                              void *cache, int64_t num_blocks, int32_t block_size,
+                              int32_t *dev_status, void *stream) {
+  g_detail.clear();
+  if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARGUMENT, "num_tokens < 0");
+  if (block_size <= 0) return fail(MLA_ERR_INVALID_ARGUMENT, "block_size %d <= 0", block_size);
+  if (num_blocks <= 0) return fail(MLA_ERR_INVALID_ARGUMENT, "num_blocks <= 0");
+  if (num_tokens == 0) return MLA_OK;
+  if (!kv_new || !slot_mapping || !cache) return fail(MLA_ERR_INVALID_ARGUMENT, "null pointer");
+  if (!aligned(kv_new, 16) || !aligned(cache, 16) || !aligned(slot_mapping, 8))
+    return fail(MLA_ERR_INVALID_ARGUMENT, "kv_new/cache must be 16-byte, slot_mapping 8-byte aligned");
+  cudaError_t e = launch_cache_append(kv_new, slot_mapping, num_tokens, cache,
+                                      num_blocks * (int64_t)block_size, dev_status,
+                                      (cudaStream_t)stream);
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_cache_append launch");
+}
+
+size_t mla_decode_workspace_size(int32_t batch, int32_t num_heads) {
+  if (batch < 0 || num_heads <= 0) return 0;
+  const int ranges = max_ranges_current();
+  if (ranges <= 0) return 0;
+  return workspace_layout(batch, num_heads, ranges).total;
+}
+
+mla_status_t mla_decode_plan(const int32_t *seq_lens, int32_t batch, int32_t num_heads,
+                             int32_t max_blocks_per_seq, int32_t block_size, void *workspace,
+                             size_t workspace_bytes, int32_t *dev_status, void *stream) {
+  g_detail.clear();
+  if (batch < 0) return fail(MLA_ERR_INVALID_ARGUMENT, "batch < 0");
+  if (num_heads != kHeads) return fail(MLA_ERR_UNSUPPORTED, "num_heads must be %d", kHeads);
+  if (!block_size_ok(block_size)) return fail(MLA_ERR_UNSUPPORTED, "block_size %d", block_size);
+  if (batch == 0) return MLA_OK;
+  if (!seq_lens || !workspace) return fail(MLA_ERR_INVALID_ARGUMENT, "null pointer");
+  if (!aligned(workspace, 256)) return fail(MLA_ERR_INVALID_ARGUMENT, "workspace alignment");
+  if (max_blocks_per_seq <= 0) return fail(MLA_ERR_INVALID_ARGUMENT, "max_blocks_per_seq <= 0");
+  const size_t need = mla_decode_workspace_size(batch, num_heads);
+  if (need == 0) return fail(MLA_ERR_CUDA, "cannot query the current device");
+  if (workspace_bytes < need)
+    return fail(MLA_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu", workspace_bytes, need);
+  cudaError_t e = launch_plan(seq_lens, batch, simt_unit_tokens(), max_blocks_per_seq,
+                              block_size, max_ranges_current(), workspace, num_heads, dev_status,
+                              (cudaStream_t)stream);
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e, "plan launch");
+}
+
+mla_status_t mla_decode_planned(const void *q, const void *cache, int64_t num_blocks,
+                                int32_t block_size, const int32_t *block_table,
+                                int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                int32_t batch, int32_t num_heads, int32_t max_seq_len,
+                                float softmax_scale, void *out, float *lse, void *workspace,
+                                size_t workspace_bytes, int32_t *dev_status, void *stream) {
+  g_detail.clear();
+  mla_status_t s = check_decode_args(q, cache, num_blocks, block_size, block_table,
+                                     max_blocks_per_seq, seq_lens, batch, num_heads, max_seq_len,
+                                     softmax_scale, out, lse, workspace, workspace_bytes);
+  if (s != MLA_OK || batch == 0) return s;
+  const int ranges = max_ranges_current();
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = launch_decode_simt(q, cache, num_blocks, block_size, block_table,
+                                     max_blocks_per_seq, batch, softmax_scale, out, lse, workspace,
+                                     ranges, dev_status, st);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  e = launch_plan_combine(workspace, batch, num_heads, ranges, out, lse, st);
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e, "combine launch");
+}
+
+mla_status_t mla_decode(const void *q, const void *cache, int64_t num_blocks, int32_t block_size,
+                        const int32_t *block_table, int32_t max_blocks_per_seq,
+                        const int32_t *seq_lens, int32_t batch, int32_t num_heads,
+                        int32_t max_seq_len, float softmax_scale, void *out, float *lse,
+                        void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                        void *stream) {
+  g_detail.clear();
+  mla_status_t s = check_decode_args(q, cache, num_blocks, block_size, block_table,
+                                     max_blocks_per_seq, seq_lens, batch, num_heads, max_seq_len,
+                                     softmax_scale, out, lse, workspace, workspace_bytes);
+  if (s != MLA_OK || batch == 0) return s;
+  s = mla_decode_plan(seq_lens, batch, num_heads, max_blocks_per_seq, block_size, workspace,
+                      workspace_bytes, dev_status, stream);
+  if (s != MLA_OK) return s;
+  return mla_decode_planned(q, cache, num_blocks, block_size, block_table, max_blocks_per_seq,
+                            seq_lens, batch, num_heads, max_seq_len, softmax_scale, out, lse,
+                            workspace, workspace_bytes, dev_status, stream);
+}
+
+mla_status_t mla_combine(const float *o_partial, const float *lse_partial,
+                         const int32_t *split_offsets, int32_t batch, int32_t num_heads,
+                         void *out, float *lse, void *stream) {
+  g_detail.clear();
+  if (batch < 0 || num_heads <= 0)
+    return fail(MLA_ERR_INVALID_ARGUMENT, "batch %d, num_heads %d", batch, num_heads);
+  if (batch == 0) return MLA_OK;
+  if (!o_partial || !lse_partial || !split_offsets || !out)
+    return fail(MLA_ERR_INVALID_ARGUMENT, "null pointer");
+  if (!aligned(o_partial, 16) || !aligned(out, 16) || !aligned(lse_partial, 4))
+    return fail(MLA_ERR_INVALID_ARGUMENT, "o_partial/out must be 16-byte aligned");
+  if (batch > 65535 * 1024) return fail(MLA_ERR_INVALID_ARGUMENT, "batch too large");
+  cudaError_t e = launch_offsets_combine(o_partial, lse_partial, split_offsets, batch, num_heads,
+                                         out, lse, (cudaStream_t)stream);
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e, "combine launch");
+}
+
+}  // extern "C"

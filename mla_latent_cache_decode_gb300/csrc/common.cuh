@@ -1,0 +1,111 @@
+// Shared device-side definitions for libmla: sizes, status reporting, the
+// split-KV plan layout in the workspace.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+constexpr int kRow = MLA_ROW_DIM;        // 576: 512 kv_c + 64 k_rope
+constexpr int kVDim = MLA_KV_LORA_RANK;  // 512
+constexpr int kHeads = MLA_NUM_HEADS;    // 128
+
+// First error wins; the kernels never trap.
+__device__ __forceinline__ void report(int32_t *dev_status, int32_t code) {
+  if (dev_status) atomicCAS(dev_status, 0, code);
+}
+
+// ---------------------------------------------------------------------------
+// Split-KV plan.
+//
+// Every request b is cut into units of kUnit tokens; unit u of the flattened
+// sequence (requests in order) is U_b + i for the i-th unit of request b.
+// The U units are split into P contiguous ranges, range p = [R_p, R_{p+1}),
+// R_p = floor(p * U / P), P = min(P_max, U).  Range p is processed by one
+// worker (a CTA pair for the tensor-core kernel).  A request whose units lie
+// in one range is written directly; a request spanning k ranges leaves k
+// fp32 partials which are merged by log-sum-exp.  Range p holds at most two
+// partial segments (its first and its last), stored in slots 2p and 2p+1:
+// the segment of request b in range p uses slot 2p if R_p >= U_b (the range
+// starts inside or at b) and 2p+1 otherwise.
+// ---------------------------------------------------------------------------
+struct PlanHeader {
+  int32_t total_units;  // U
+  int32_t num_ranges;   // P (0 when U == 0)
+  int32_t max_ranges;   // P_max the plan was made for
+  int32_t batch;
+  int32_t unit_tokens;
+  int32_t max_blocks_per_seq;
+  int32_t block_size;
+  int32_t pad;
+};
+
+// Workspace layout (all offsets 256-byte aligned):
+//   PlanHeader
+//   int32 seq_len[B]          clamped lengths
+//   int32 unit_prefix[B + 1]  U_b
+//   int32 range_first[P_max]  first request with units in range p
+//   int32 counters[B * 2]     split arrival counters (left at zero)
+//   fp32 lse_part[2 * P_max * H]
+//   fp32 o_part[2 * P_max * H * 512]
+struct WorkspaceLayout {
+  size_t seq_len, unit_prefix, range_first, counters, lse_part, o_part, total;
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+__host__ __device__ inline WorkspaceLayout workspace_layout(int batch, int heads, int max_ranges) {
+  WorkspaceLayout w;
+  size_t o = align256(sizeof(PlanHeader));
+  w.seq_len = o;      o = align256(o + sizeof(int32_t) * (size_t)batch);
+  w.unit_prefix = o;  o = align256(o + sizeof(int32_t) * ((size_t)batch + 1));
+  w.range_first = o;  o = align256(o + sizeof(int32_t) * ((size_t)max_ranges + 1));
+  w.counters = o;     o = align256(o + sizeof(int32_t) * 2 * (size_t)batch);
+  w.lse_part = o;     o = align256(o + sizeof(float) * 2 * (size_t)max_ranges * heads);
+  w.o_part = o;       o = align256(o + sizeof(float) * 2 * (size_t)max_ranges * heads * kVDim);
+  w.total = o;
+  return w;
+}
+
+struct PlanView {
+  const PlanHeader *hdr;
+  const int32_t *seq_len;
+  const int32_t *unit_prefix;
+  const int32_t *range_first;
+  int32_t *counters;
+  float *lse_part;
+  float *o_part;
+};
+
+__host__ __device__ inline PlanView plan_view(void *ws, int batch, int heads, int max_ranges) {
+  WorkspaceLayout l = workspace_layout(batch, heads, max_ranges);
+  char *b = (char *)ws;
+  PlanView v;
+  v.hdr = (const PlanHeader *)b;
+  v.seq_len = (const int32_t *)(b + l.seq_len);
+  v.unit_prefix = (const int32_t *)(b + l.unit_prefix);
+  v.range_first = (const int32_t *)(b + l.range_first);
+  v.counters = (int32_t *)(b + l.counters);
+  v.lse_part = (float *)(b + l.lse_part);
+  v.o_part = (float *)(b + l.o_part);
+  return v;
+}
+
+__host__ __device__ inline int32_t range_begin(int32_t p, int32_t U, int32_t P) {
+  return (int32_t)(((int64_t)p * U) / P);
+}
+
+// Range holding unit u (0 <= u < U): the largest p with R_p <= u.
+__host__ __device__ inline int32_t range_of(int32_t u, int32_t U, int32_t P) {
+  return (int32_t)((((int64_t)u + 1) * P - 1) / U);
+}
+
+__host__ __device__ inline int32_t partial_slot(int32_t p, int32_t U, int32_t P, int32_t Ub) {
+  return 2 * p + (range_begin(p, U, P) < Ub ? 1 : 0);
+}
+
+}  // namespace mla

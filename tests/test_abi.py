@@ -1,0 +1,72 @@
+"""C-ABI library checks that need no GPU: it loads, exports every declared
+symbol, and rejects bad arguments on the host before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mla_latent_cache_decode_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"\b(mla_\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 9, names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_binding_names_match_header():
+    import mla_latent_cache_decode_gb300 as mla
+    assert set(mla.EXPORTED) == set(declared_functions())
+
+
+def test_status_strings_and_version(lib):
+    lib.mla_status_string.restype = ctypes.c_char_p
+    lib.mla_abi_version.restype = ctypes.c_int
+    assert lib.mla_abi_version() == 1
+    names = [lib.mla_status_string(i).decode() for i in range(7)]
+    assert names[0] == "MLA_OK" and names[6] == "MLA_ERR_DEVICE_TIMEOUT"
+    assert lib.mla_status_string(99).decode() == "MLA_ERR_UNKNOWN"
+
+
+def test_host_validation_before_any_launch(lib):
+    P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    lib.mla_decode.argtypes = [P, P, i64, i32, P, i32, P, i32, i32, i32, f32, P, P, P, sz, P, P]
+    lib.mla_decode.restype = ctypes.c_int
+    lib.mla_last_error_detail.restype = ctypes.c_char_p
+    lib.mla_cache_append.argtypes = [P, P, i64, P, i64, i32, P, P]
+    lib.mla_cache_append.restype = ctypes.c_int
+    lib.mla_combine.argtypes = [P, P, P, i32, i32, P, P, P]
+    lib.mla_combine.restype = ctypes.c_int
+    args = lambda batch, heads, bs: (None, None, 1, bs, None, 1, None, batch, heads, 1, 0.1,
+                                     None, None, None, 0, None, None)
+    assert lib.mla_decode(*args(-1, 128, 64)) == 1
+    assert lib.mla_decode(*args(2, 64, 64)) == 2          # heads other than 128
+    assert b"num_heads" in lib.mla_last_error_detail()
+    assert lib.mla_decode(*args(2, 128, 48)) == 2         # unsupported page size
+    assert lib.mla_decode(*args(2, 128, 0)) == 1
+    assert lib.mla_decode(*args(0, 128, 64)) == 0         # empty batch: valid no-op
+    assert lib.mla_decode(*args(2, 128, 64)) == 1         # null pointers
+    assert lib.mla_cache_append(None, None, 0, None, 1, 16, None, None) == 0
+    assert lib.mla_cache_append(None, None, 3, None, 1, 16, None, None) == 1
+    assert lib.mla_cache_append(None, None, -1, None, 1, 16, None, None) == 1
+    assert lib.mla_combine(None, None, None, 0, 128, None, None, None) == 0
+    assert lib.mla_combine(None, None, None, 2, 128, None, None, None) == 1

@@ -1,0 +1,408 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Small cases compare every output element; the full-size workloads (in the
+launch configuration the benchmark times) compare sampled requests the oracle
+can compute.  Bar: rel-L2 <= 5e-3 and max-abs <= 1e-2 * max|ref| for the bf16
+output, lse within 2e-3, append bit-exact.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import mla_inputs as mi
+import oracle
+from gpu_helpers import (assert_close, assert_lse_close, dev, dev_bf16, host_bits, host_f64)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def mla():
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    import mla_latent_cache_decode_gb300 as m
+    return m
+
+
+def run_layer(mla, d, *, append=True, planned=False, heads=128):
+    """Append (optional) + decode one host layer on the GPU; returns torch results."""
+    cache = dev_bf16(d["cache"])
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if append:
+        mla.mla_cache_append(dev_bf16(d["kv_new"]), dev(d["slot_mapping"], torch.int64), cache,
+                             dev_status=status)
+    B = d["q"].shape[0]
+    out = torch.full((B, heads, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, heads), float("nan"), dtype=torch.float32, device="cuda")
+    q = dev_bf16(d["q"])
+    bt = dev(d["block_table"], torch.int32)
+    sl = dev(d["seq_lens"], torch.int32)
+    ws = mla.make_workspace(B)
+    if planned:
+        mla.mla_decode_plan(sl, bt, d["cache"].shape[1], ws, dev_status=status)
+        mla.mla_decode_planned(q, cache, bt, sl, d["softmax_scale"], out, lse, workspace=ws,
+                               dev_status=status)
+    else:
+        mla.mla_decode(q, cache, bt, sl, d["softmax_scale"], out, lse, workspace=ws,
+                       dev_status=status)
+    torch.cuda.synchronize()
+    return cache, out, lse, int(status.item())
+
+
+def oracle_layer(d, append=True):
+    cache = d["cache"].copy()
+    if append:
+        oracle.append(d["kv_new"], d["slot_mapping"], cache)
+    out, lse = oracle.decode(d["q"], cache, d["block_table"], d["seq_lens"], d["softmax_scale"])
+    return cache, out, lse
+
+
+# ----------------------------------------------------------------------------- append
+
+def test_append_bit_exact(mla):
+    w = mi.workload(1)
+    d = mi.make_host_layer(w, mi.rng_for(1))
+    cache, *_ = run_layer(mla, d)
+    ref_cache, _, _ = oracle_layer(d)
+    assert np.array_equal(host_bits(cache), ref_cache)
+
+
+def test_append_skips_minus_one_and_flags_out_of_range(mla):
+    rng = np.random.default_rng(5)
+    cache_h = mi.f32_to_bf16_bits(rng.standard_normal((6, 16, 576), dtype=np.float32))
+    kv = mi.f32_to_bf16_bits(rng.standard_normal((5, 576), dtype=np.float32))
+    slots = np.array([3, -1, 95, 96, 40], np.int64)   # 96 = 6*16 is outside the pool
+    cache = dev_bf16(cache_h)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.mla_cache_append(dev_bf16(kv), dev(slots, torch.int64), cache, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 5
+    ref = cache_h.copy()
+    ok = slots.copy()
+    ok[3] = -1
+    oracle.append(kv, ok, ref)
+    assert np.array_equal(host_bits(cache), ref)
+
+
+def test_append_many_tokens(mla):
+    rng = np.random.default_rng(6)
+    NB, BS, T = 300, 64, 5000
+    cache_h = mi.f32_to_bf16_bits(rng.standard_normal((NB, BS, 576), dtype=np.float32))
+    kv = mi.f32_to_bf16_bits(rng.standard_normal((T, 576), dtype=np.float32))
+    slots = rng.permutation(NB * BS)[:T].astype(np.int64)
+    cache = dev_bf16(cache_h)
+    mla.mla_cache_append(dev_bf16(kv), dev(slots, torch.int64), cache)
+    torch.cuda.synchronize()
+    oracle.append(kv, slots, cache_h)
+    assert np.array_equal(host_bits(cache), cache_h)
+
+
+# ----------------------------------------------------------------------------- config 1
+
+@pytest.mark.parametrize("q_kind", ["normal", "sharp"])
+@pytest.mark.parametrize("planned", [False, True])
+def test_config1_after_append(mla, q_kind, planned):
+    w = mi.workload(1)
+    d = mi.make_host_layer(w, mi.rng_for(1), q_kind=q_kind)
+    cache, out, lse, st = run_layer(mla, d, planned=planned)
+    assert st == 0
+    ref_cache, ref, ref_lse = oracle_layer(d)
+    assert np.array_equal(host_bits(cache), ref_cache)
+    assert_close(host_f64(out), ref, f"config1 {q_kind}")
+    assert_lse_close(lse.cpu().numpy(), ref_lse)
+
+
+@pytest.mark.parametrize("q_kind", ["normal", "sharp"])
+def test_config1_before_append_lengths_1_17_64_200(mla, q_kind):
+    w = mi.workload(1)
+    d = mi.make_host_layer(w, mi.rng_for(1), q_kind=q_kind)
+    d["seq_lens"] = np.array(w.extra["pre_append_lens"], np.int32)
+    _, out, lse, st = run_layer(mla, d, append=False)
+    assert st == 0
+    _, ref, ref_lse = oracle_layer(d, append=False)
+    assert_close(host_f64(out), ref, f"config1 pre-append {q_kind}")
+    assert_lse_close(lse.cpu().numpy(), ref_lse)
+    # 1-token context: output is exactly the kv_c part of the only row
+    row0 = mi.gather_rows(d["cache"], d["block_table"], 0, 1, 16)[0]
+    got0 = host_bits(out)[0]
+    assert np.array_equal(got0, np.broadcast_to(row0[:512], got0.shape))
+
+
+# ----------------------------------------------------------------------------- invariants
+
+def test_one_token_contexts_bit_exact(mla):
+    w = mi.custom_workload([1] * 37, block_size=16, append=False, pool_factor=3.0)
+    d = mi.make_host_layer(w, np.random.default_rng(8), q_kind="sharp")
+    _, out, lse, st = run_layer(mla, d, append=False)
+    assert st == 0
+    got = host_bits(out)
+    for b in range(37):
+        row = mi.gather_rows(d["cache"], d["block_table"], b, 1, 16)[0]
+        assert np.array_equal(got[b], np.broadcast_to(row[:512], got[b].shape))
+
+
+def test_block_permutation_bit_exact_and_repeatable(mla):
+    w = mi.custom_workload([300, 1000, 77, 2048], block_size=32, append=False, pool_factor=1.7)
+    d = mi.make_host_layer(w, np.random.default_rng(9), q_kind="sharp")
+    _, out0, lse0, _ = run_layer(mla, d, append=False)
+    _, out0b, lse0b, _ = run_layer(mla, d, append=False)
+    assert torch.equal(out0.view(torch.int16), out0b.view(torch.int16)) and torch.equal(lse0, lse0b)
+    NB = d["cache"].shape[0]
+    perm = np.random.default_rng(10).permutation(NB)
+    d2 = dict(d)
+    d2["cache"] = np.empty_like(d["cache"])
+    d2["cache"][perm] = d["cache"]
+    d2["block_table"] = np.where(d["block_table"] >= 0, perm[np.maximum(d["block_table"], 0)],
+                                 -1).astype(np.int32)
+    _, out1, lse1, _ = run_layer(mla, d2, append=False)
+    assert torch.equal(out0.view(torch.int16), out1.view(torch.int16)) and torch.equal(lse0, lse1)
+
+
+# ----------------------------------------------------------------------------- edge cases
+
+def test_empty_batch_is_a_noop(mla):
+    q = torch.empty((0, 128, 576), dtype=torch.bfloat16, device="cuda")
+    cache = torch.zeros((4, 16, 576), dtype=torch.bfloat16, device="cuda")
+    bt = torch.zeros((0, 1), dtype=torch.int32, device="cuda")
+    sl = torch.zeros((0,), dtype=torch.int32, device="cuda")
+    out = torch.empty((0, 128, 512), dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    mla.mla_decode(q, cache, bt, sl, 0.1, out, workspace=ws)
+    torch.cuda.synchronize()
+
+
+def test_zero_length_requests(mla):
+    lens = [0, 5, 0, 130, 0]
+    w = mi.custom_workload([max(L, 1) for L in lens], block_size=16, append=False, pool_factor=2)
+    d = mi.make_host_layer(w, np.random.default_rng(11))
+    d["seq_lens"] = np.array(lens, np.int32)
+    _, out, lse, st = run_layer(mla, d, append=False)
+    assert st == 0
+    _, ref, ref_lse = oracle_layer(d, append=False)
+    o = host_f64(out)
+    for b in (0, 2, 4):
+        assert (o[b] == 0).all()
+    assert_close(o[[1, 3]], ref[[1, 3]])
+    assert_lse_close(lse.cpu().numpy(), ref_lse)
+
+
+def test_all_empty_batch(mla):
+    w = mi.custom_workload([1, 1, 1], block_size=16, append=False, pool_factor=2)
+    d = mi.make_host_layer(w, np.random.default_rng(12))
+    d["seq_lens"] = np.zeros(3, np.int32)
+    _, out, lse, st = run_layer(mla, d, append=False)
+    assert st == 0 and (host_f64(out) == 0).all() and torch.isinf(lse).all()
+
+
+@pytest.mark.parametrize("block_size", [16, 32, 64, 128, 256])
+def test_block_sizes_ragged(mla, block_size):
+    lens = [1, 31, 32, 33, 63, 64, 65, 127, 129, 255, 257, 600, 1023, 1500]
+    w = mi.custom_workload(lens, block_size=block_size, append=True, pool_factor=1.3)
+    d = mi.make_host_layer(w, np.random.default_rng(block_size), q_kind="sharp")
+    cache, out, lse, st = run_layer(mla, d)
+    assert st == 0
+    ref_cache, ref, ref_lse = oracle_layer(d)
+    assert np.array_equal(host_bits(cache), ref_cache)
+    assert_close(host_f64(out), ref, f"BS={block_size}")
+    assert_lse_close(lse.cpu().numpy(), ref_lse)
+
+
+def test_many_short_requests(mla):
+    rng = np.random.default_rng(13)
+    lens = rng.integers(1, 40, size=700).tolist()
+    w = mi.custom_workload(lens, block_size=16, append=True, pool_factor=1.2)
+    d = mi.make_host_layer(w, rng)
+    cache, out, lse, st = run_layer(mla, d)
+    assert st == 0
+    _, ref, ref_lse = oracle_layer(d)
+    assert_close(host_f64(out), ref, "700 short requests")
+    assert_lse_close(lse.cpu().numpy(), ref_lse)
+
+
+def test_one_long_request_among_short(mla):
+    lens = [9000, 3, 70, 1]
+    w = mi.custom_workload(lens, block_size=64, append=True, pool_factor=1.1)
+    d = mi.make_host_layer(w, np.random.default_rng(14), q_kind="sharp")
+    cache, out, lse, st = run_layer(mla, d)
+    assert st == 0
+    _, ref, ref_lse = oracle_layer(d)
+    assert_close(host_f64(out), ref, "long + short")
+    assert_lse_close(lse.cpu().numpy(), ref_lse)
+
+
+def test_bad_block_id_is_flagged_not_faulted(mla):
+    w = mi.custom_workload([40, 40], block_size=16, append=False, pool_factor=1.0)
+    d = mi.make_host_layer(w, np.random.default_rng(15))
+    d["block_table"] = d["block_table"].copy()
+    d["block_table"][1, 1] = 10_000_000
+    _, out, lse, st = run_layer(mla, d, append=False)
+    assert st == 5
+    _, ref, _ = oracle_layer(dict(d, q=d["q"][:1], block_table=d["block_table"][:1],
+                                  seq_lens=d["seq_lens"][:1]), append=False)
+    assert_close(host_f64(out)[:1], ref, "request without the bad entry")
+
+
+def test_seq_len_longer_than_table_is_flagged(mla):
+    w = mi.custom_workload([40], block_size=16, append=False, pool_factor=1.0)
+    d = mi.make_host_layer(w, np.random.default_rng(16))
+    d["seq_lens"] = np.array([10_000], np.int32)
+    _, out, lse, st = run_layer(mla, d, append=False)
+    assert st == 5
+
+
+def test_host_validation_errors(mla):
+    q = torch.zeros((1, 128, 576), dtype=torch.bfloat16, device="cuda")
+    cache = torch.zeros((4, 16, 576), dtype=torch.bfloat16, device="cuda")
+    bt = torch.zeros((1, 4), dtype=torch.int32, device="cuda")
+    sl = torch.ones((1,), dtype=torch.int32, device="cuda")
+    out = torch.empty((1, 128, 512), dtype=torch.bfloat16, device="cuda")
+    small = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(mla.MlaError) as e:
+        mla.mla_decode(q, cache, bt, sl, 0.1, out, workspace=small)
+    assert e.value.status == 3
+    with pytest.raises(mla.MlaError) as e:
+        mla.mla_decode(q, cache, bt, sl, 0.1, out, max_seq_len=65)
+    assert e.value.status == 1
+    with pytest.raises(mla.MlaError) as e:
+        mla.mla_decode(q, cache, bt, sl, float("inf"), out)
+    assert e.value.status == 1
+
+
+# ----------------------------------------------------------------------------- combine
+
+def test_combine_against_oracle(mla):
+    rng = np.random.default_rng(17)
+    counts = [3, 1, 0, 5, 2]
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    W, H = int(offs[-1]), 128
+    o = rng.standard_normal((W, H, 512)).astype(np.float32)
+    l = (rng.standard_normal((W, H)) * 3).astype(np.float32)
+    l[4, :7] = -np.inf
+    out = torch.empty((5, H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((5, H), dtype=torch.float32, device="cuda")
+    mla.mla_combine(dev(o, torch.float32), dev(l, torch.float32), dev(offs, torch.int32), out, lse)
+    torch.cuda.synchronize()
+    ref, ref_lse = oracle.combine(o.astype(np.float64), l.astype(np.float64), offs)
+    got = host_f64(out)
+    assert (got[2] == 0).all() and torch.isinf(lse[2]).all()
+    keep = [0, 1, 3, 4]
+    assert_close(got[keep], ref[keep], "combine")
+    assert_lse_close(lse.cpu().numpy()[keep], ref_lse[keep])
+
+
+# ----------------------------------------------------------------------------- full-size workloads
+
+def _device_layer_and_host(w, layer, q_kind="normal", block_table=None):
+    dl = mi.make_device_layer(w, layer, "cuda", q_kind=q_kind, block_table=block_table)
+    host = dict(q=mi.to_bits(dl["q"]), cache=mi.to_bits(dl["cache"]),
+                block_table=dl["block_table_host"], seq_lens=dl["seq_lens"].cpu().numpy(),
+                kv_new=mi.to_bits(dl["kv_new"]), slot_mapping=dl["slot_mapping"].cpu().numpy(),
+                softmax_scale=dl["softmax_scale"])
+    return dl, host
+
+
+def _oracle_sample(host, reqs, heads=None):
+    cache = host["cache"].copy()
+    oracle.append(host["kv_new"], host["slot_mapping"], cache)
+    q = host["q"][reqs]
+    if heads is not None:
+        q = q[:, heads]
+    return oracle.decode(q, cache, host["block_table"][reqs], host["seq_lens"][reqs],
+                         host["softmax_scale"])
+
+
+def _gpu_layer(mla, dl, ws, status, planned):
+    B = dl["q"].shape[0]
+    out = torch.empty((B, 128, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, 128), dtype=torch.float32, device="cuda")
+    mla.mla_cache_append(dl["kv_new"], dl["slot_mapping"], dl["cache"], dev_status=status)
+    fn = mla.mla_decode_planned if planned else mla.mla_decode
+    fn(dl["q"], dl["cache"], dl["block_table"], dl["seq_lens"], dl["softmax_scale"], out, lse,
+       workspace=ws, dev_status=status)
+    return out, lse
+
+
+@pytest.mark.parametrize("q_kind", ["normal", "sharp"])
+def test_config2_layer_b64x4096_sampled(mla, q_kind):
+    w = mi.workload(2)
+    dl, host = _device_layer_and_host(w, 0, q_kind)
+    ws = mla.make_workspace(w.batch)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = _gpu_layer(mla, dl, ws, status, planned=False)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    reqs = [0, 17, 40, 63]
+    ref, ref_lse = _oracle_sample(host, reqs)
+    assert_close(host_f64(out)[reqs], ref, f"config2 {q_kind}")
+    assert_lse_close(lse.cpu().numpy()[reqs], ref_lse)
+
+
+def test_config4_skewed_sampled(mla):
+    w = mi.workload(4)
+    dl, host = _device_layer_and_host(w, 0, "sharp")
+    ws = mla.make_workspace(w.batch)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = _gpu_layer(mla, dl, ws, status, planned=False)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    heads = [0, 37, 64, 127]
+    ref, ref_lse = _oracle_sample(host, [0], heads)     # the 131072-token request
+    assert_close(host_f64(out)[0, heads], ref[0], "config4 long request")
+    assert_lse_close(lse.cpu().numpy()[0, heads], ref_lse[0])
+    ref, ref_lse = _oracle_sample(host, [1, 7])
+    assert_close(host_f64(out)[[1, 7]], ref, "config4 short requests")
+
+
+def test_config5_mixed_fragmented_sampled(mla):
+    w = mi.workload(5)
+    bt = mi.make_block_table(mi.rng_for(5, 0, 1), w.seq_lens, w.block_size, w.num_blocks())
+    ws = mla.make_workspace(w.batch)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lens = np.array(w.seq_lens)
+    reqs = sorted({int(lens.argmin()), int(lens.argmax()), 0, 100, 255})
+    for layer in range(w.layers):
+        dl, host = _device_layer_and_host(w, layer, block_table=bt)
+        if layer == 0:
+            seq = dl["seq_lens"]
+            mla.mla_decode_plan(seq, dl["block_table"], w.block_size, ws, dev_status=status)
+        out, lse = _gpu_layer(mla, dl, ws, status, planned=True)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        if layer in (0, w.layers - 1):
+            ref, ref_lse = _oracle_sample(host, reqs)
+            assert_close(host_f64(out)[reqs], ref, f"config5 layer {layer}")
+            assert_lse_close(lse.cpu().numpy()[reqs], ref_lse)
+        del dl, host
+
+
+def test_config3_dp_rank_61_layers_sampled(mla):
+    """The benchmark's launch configuration: one plan per step, then append +
+    planned decode per layer, each layer with its own cache, shared table."""
+    w = mi.workload(3)
+    bt = mi.make_block_table(mi.rng_for(3, 0, 1), w.seq_lens, w.block_size, w.num_blocks())
+    ws = mla.make_workspace(w.batch)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sample_layers = {0, 29, 60}
+    reqs = [0, 11, 19]
+    for layer in range(w.layers):
+        dl = mi.make_device_layer(w, layer, "cuda", block_table=bt)
+        if layer == 0:
+            mla.mla_decode_plan(dl["seq_lens"], dl["block_table"], w.block_size, ws,
+                                dev_status=status)
+        host = None
+        if layer in sample_layers:
+            host = dict(q=mi.to_bits(dl["q"]), cache=mi.to_bits(dl["cache"]), block_table=bt,
+                        seq_lens=dl["seq_lens"].cpu().numpy(), kv_new=mi.to_bits(dl["kv_new"]),
+                        slot_mapping=dl["slot_mapping"].cpu().numpy(),
+                        softmax_scale=dl["softmax_scale"])
+        out, lse = _gpu_layer(mla, dl, ws, status, planned=True)
+        if host is not None:
+            torch.cuda.synchronize()
+            ref, ref_lse = _oracle_sample(host, reqs)
+            assert_close(host_f64(out)[reqs], ref, f"config3 layer {layer}")
+            assert_lse_close(lse.cpu().numpy()[reqs], ref_lse)
+        del dl
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
