@@ -191,6 +191,47 @@ mla_status_t mla_combine(const float *o_partial, const float *lse_partial,
                          const int32_t *split_offsets, int32_t batch, int32_t num_heads,
                          void *out, float *lse, void *stream);
 
+/*
+ * mla_decode_noalloc — mla_decode for callers that cannot allocate device
+ * memory.  The pages have no counterpart to this entry point; it exists for
+ * users of this library.
+ *
+ * Some callers cannot call cudaMalloc (or any allocating routine) at decode
+ * time: code running inside a host framework that owns all device memory and
+ * hands a plugin only its inputs and outputs, or a latency-critical serving
+ * path that must not touch the allocator (and so cannot fail with
+ * out-of-memory) in the middle of a step.  Such a caller cannot provide the
+ * workspace mla_decode needs.  This entry point takes the same arguments as
+ * mla_decode minus the workspace, and uses instead a fixed scratch array of
+ * MLA_NOALLOC_SCRATCH_BYTES (16 MiB) compiled into the library as a
+ * file-scope device array: every GPU that loads the library holds those
+ * 16 MiB until the process exits.  It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *
+ * Limits: batch <= MLA_NOALLOC_MAX_BATCH (8192), else
+ * MLA_ERR_INVALID_ARGUMENT with an explanatory detail.  Because the scratch
+ * holds fewer split partials than a full workspace, long contexts are spread
+ * over fewer SMs than with mla_decode, which can make it slower; results agree
+ * with mla_decode within the library's tolerance (the split points differ, so
+ * fp32 rounding differs).
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call shares the one array and overwrites
+ * what the previous call left there (each call re-plans and re-zeroes what
+ * must start at zero), so calls whose kernels overlap on the GPU — on
+ * different streams, or from different host threads — race and give
+ * undefined results: serialise them.
+ */
+#define MLA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+#define MLA_NOALLOC_MAX_BATCH 8192
+mla_status_t mla_decode_noalloc(const void *q, const void *cache, int64_t num_blocks,
+                                int32_t block_size, const int32_t *block_table,
+                                int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                int32_t batch, int32_t num_heads, int32_t max_seq_len,
+                                float softmax_scale, void *out, float *lse, int32_t *dev_status,
+                                void *stream);
+
 #ifdef __cplusplus
 }
 #endif

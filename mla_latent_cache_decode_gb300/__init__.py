@@ -28,7 +28,7 @@ STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARGUMENT", 2: "MLA_ERR_UNSUPPORTED",
           6: "MLA_ERR_DEVICE_TIMEOUT"}
 EXPORTED = ("mla_status_string", "mla_last_error_detail", "mla_abi_version", "mla_cache_append",
             "mla_decode_workspace_size", "mla_decode_plan", "mla_decode", "mla_decode_planned",
-            "mla_combine")
+            "mla_combine", "mla_decode_noalloc")
 
 
 class MlaError(RuntimeError):
@@ -64,6 +64,8 @@ def _load():
     lib.mla_decode_planned.restype = ctypes.c_int
     lib.mla_combine.argtypes = [P, P, P, i32, i32, P, P, P]
     lib.mla_combine.restype = ctypes.c_int
+    lib.mla_decode_noalloc.argtypes = [P, P, i64, i32, P, i32, P, i32, i32, i32, f32, P, P, P, P]
+    lib.mla_decode_noalloc.restype = ctypes.c_int
     return lib
 
 
@@ -207,4 +209,27 @@ def mla_combine(o_partial, lse_partial, split_offsets, out, lse=None, stream=Non
         raise ValueError("shape mismatch")
     _check(get_lib().mla_combine(_ptr(o_partial), _ptr(lse_partial), _ptr(split_offsets), B, H,
                            _ptr(out), _ptr(lse), _stream(stream)))
+    return out
+
+
+def mla_decode_noalloc(q, cache, block_table, seq_lens, softmax_scale, out, lse=None,
+                       max_seq_len=None, dev_status=None, stream=None):
+    """mla_decode without a workspace, for callers that cannot allocate device
+    memory: the library's fixed 16 MiB scratch array stands in for it (batch
+    <= 8192; calls must not overlap on the GPU)."""
+    import torch
+    _need(q, torch.bfloat16, 3, "q")
+    _need(cache, torch.bfloat16, 3, "cache")
+    _need(block_table, torch.int32, 2, "block_table")
+    _need(seq_lens, torch.int32, 1, "seq_lens")
+    _need(out, torch.bfloat16, 3, "out")
+    if lse is not None:
+        _need(lse, torch.float32, 2, "lse")
+    B, H, _ = q.shape
+    if max_seq_len is None:
+        max_seq_len = block_table.shape[1] * cache.shape[1]
+    _check(get_lib().mla_decode_noalloc(
+        _ptr(q), _ptr(cache), cache.shape[0], cache.shape[1], _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), B, H, int(max_seq_len), float(softmax_scale),
+        _ptr(out), _ptr(lse), _ptr(dev_status), _stream(stream)))
     return out

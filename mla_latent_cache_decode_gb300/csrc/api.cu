@@ -109,6 +109,10 @@ mla_status_t check_decode_args(const void *q, const void *cache, int64_t num_blo
 }
 
 }  // namespace
+
+// Failure reporting for the fixed-scratch entry point (noalloc.cu).
+mla_status_t noalloc_fail(mla_status_t s, const char *msg) { return fail(s, "%s", msg); }
+
 }  // namespace mla
 
 using namespace mla;

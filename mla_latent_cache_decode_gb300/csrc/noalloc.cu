@@ -1,0 +1,117 @@
+// mla_decode_noalloc: the decode entry point for callers that cannot allocate
+// device memory.  Its scratch (split plan + partial results) lives in a fixed,
+// file-scope device array instead of a caller-provided workspace.
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace mla {
+cudaError_t launch_plan(const int32_t *seq_lens, int32_t batch, int32_t unit_tokens,
+                        int32_t max_blocks_per_seq, int32_t block_size, int32_t max_ranges,
+                        void *ws, int32_t heads, int32_t *dev_status, cudaStream_t stream);
+cudaError_t launch_plan_combine(void *ws, int32_t batch, int32_t heads, int32_t max_ranges,
+                                void *out, float *lse, cudaStream_t stream);
+int simt_unit_tokens();
+cudaError_t launch_decode_simt(const void *q, const void *cache, int64_t num_blocks,
+                               int32_t block_size, const int32_t *block_table,
+                               int32_t max_blocks_per_seq, int32_t batch, float softmax_scale,
+                               void *out, float *lse, void *ws, int32_t max_ranges,
+                               int32_t *dev_status, cudaStream_t stream);
+mla_status_t noalloc_fail(mla_status_t s, const char *msg);
+}  // namespace mla
+
+// Every GPU that loads this library holds this array until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MLA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+// Device address of g_noalloc_scratch, looked up once per device with that
+// device current.  In host code the symbol itself is only a host-side
+// stand-in, never a device address.
+void *scratch_address(int *err) {
+  static std::mutex mu;
+  static void *addr[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) {
+    *err = 1;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) {
+      *err = 2;
+      return nullptr;
+    }
+    addr[dev] = p;
+  }
+  *err = 0;
+  return addr[dev];
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  return n;
+}
+
+}  // namespace
+
+using namespace mla;
+
+extern "C" mla_status_t mla_decode_noalloc(const void *q, const void *cache, int64_t num_blocks,
+                                           int32_t block_size, const int32_t *block_table,
+                                           int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                           int32_t batch, int32_t num_heads, int32_t max_seq_len,
+                                           float softmax_scale, void *out, float *lse,
+                                           int32_t *dev_status, void *stream) {
+  noalloc_fail(MLA_OK, "");
+  if (batch > MLA_NOALLOC_MAX_BATCH)
+    return noalloc_fail(MLA_ERR_INVALID_ARGUMENT,
+                        "batch exceeds MLA_NOALLOC_MAX_BATCH (the fixed scratch holds the plan "
+                        "for at most 8192 requests)");
+  if (batch < 0 || num_heads != kHeads || block_size <= 0)
+    return noalloc_fail(batch < 0 || block_size <= 0 ? MLA_ERR_INVALID_ARGUMENT
+                                                      : MLA_ERR_UNSUPPORTED,
+                        "batch >= 0, num_heads == 128 and block_size > 0 are required");
+  if (batch == 0) return MLA_OK;
+  // Ranges of the split plan: one per SM, as many as the fixed scratch holds.
+  const int sms = sm_count();
+  if (sms <= 0) return noalloc_fail(MLA_ERR_CUDA, "cannot query the current device");
+  int ranges = sms;
+  while (ranges > 1 && workspace_layout(batch, kHeads, ranges).total > MLA_NOALLOC_SCRATCH_BYTES)
+    --ranges;
+  if (workspace_layout(batch, kHeads, ranges).total > MLA_NOALLOC_SCRATCH_BYTES)
+    return noalloc_fail(MLA_ERR_INVALID_ARGUMENT, "batch too large for the fixed scratch");
+  if (!q || !cache || !block_table || !seq_lens || !out)
+    return noalloc_fail(MLA_ERR_INVALID_ARGUMENT, "null pointer argument");
+  if (((uintptr_t)q | (uintptr_t)cache | (uintptr_t)out) % 16)
+    return noalloc_fail(MLA_ERR_INVALID_ARGUMENT, "q, cache and out must be 16-byte aligned");
+  if (((uintptr_t)block_table | (uintptr_t)seq_lens | (uintptr_t)lse) % 4)
+    return noalloc_fail(MLA_ERR_INVALID_ARGUMENT, "block_table, seq_lens, lse: 4-byte alignment");
+  if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128 &&
+      block_size != 256)
+    return noalloc_fail(MLA_ERR_UNSUPPORTED, "block_size not in {16,32,64,128,256}");
+  if (num_blocks <= 0 || num_blocks > (int64_t)INT32_MAX || max_blocks_per_seq <= 0 ||
+      (int64_t)max_blocks_per_seq * block_size > (int64_t)INT32_MAX / 2 || max_seq_len < 0 ||
+      (int64_t)max_seq_len > (int64_t)max_blocks_per_seq * block_size)
+    return noalloc_fail(MLA_ERR_INVALID_ARGUMENT, "bad num_blocks, table width or max_seq_len");
+  if (!(softmax_scale == softmax_scale) || softmax_scale == INFINITY || softmax_scale == -INFINITY)
+    return noalloc_fail(MLA_ERR_INVALID_ARGUMENT, "softmax_scale is not finite");
+  int err = 0;
+  void *ws = scratch_address(&err);
+  if (!ws) return noalloc_fail(MLA_ERR_CUDA, "cudaGetSymbolAddress of the scratch array failed");
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = launch_plan(seq_lens, batch, simt_unit_tokens(), max_blocks_per_seq, block_size,
+                              ranges, ws, num_heads, dev_status, st);
+  if (e == cudaSuccess)
+    e = launch_decode_simt(q, cache, num_blocks, block_size, block_table, max_blocks_per_seq,
+                           batch, softmax_scale, out, lse, ws, ranges, dev_status, st);
+  if (e == cudaSuccess) e = launch_plan_combine(ws, batch, num_heads, ranges, out, lse, st);
+  if (e != cudaSuccess) return noalloc_fail(MLA_ERR_CUDA, cudaGetErrorString(e));
+  return MLA_OK;
+}

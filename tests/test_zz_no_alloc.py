@@ -1,0 +1,75 @@
+"""mla_decode_noalloc: the decode entry point for callers that cannot allocate
+device memory (a host framework that owns all device memory and gives a plugin
+only its inputs and outputs, or a serving path that must not touch the
+allocator mid-step).  It uses the library's fixed scratch array instead of a
+workspace, so its results must match mla_decode's within the parity tolerance,
+also on a second call right after the first (the scratch keeps the previous
+call's contents and must not leak into the next result).
+
+Collected last on purpose, and self-contained so it also passes alone in a
+fresh process.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import mla_inputs as mi
+from gpu_helpers import assert_close, assert_lse_close, dev, dev_bf16, host_f64
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def _inputs(lens, block_size, seed, q_kind):
+    w = mi.custom_workload(lens, block_size=block_size, append=False, pool_factor=1.3)
+    d = mi.make_host_layer(w, np.random.default_rng(seed), q_kind=q_kind)
+    return dict(q=dev_bf16(d["q"]), cache=dev_bf16(d["cache"]),
+                bt=dev(d["block_table"], torch.int32), sl=dev(d["seq_lens"], torch.int32),
+                scale=d["softmax_scale"], B=len(lens))
+
+
+def _noalloc_via_c_abi(lib, x, out, lse, status):
+    stream = torch.cuda.current_stream().cuda_stream
+    return lib.mla_decode_noalloc(
+        ctypes.c_void_p(x["q"].data_ptr()), ctypes.c_void_p(x["cache"].data_ptr()),
+        x["cache"].shape[0], x["cache"].shape[1], ctypes.c_void_p(x["bt"].data_ptr()),
+        x["bt"].shape[1], ctypes.c_void_p(x["sl"].data_ptr()), x["B"], 128,
+        x["bt"].shape[1] * x["cache"].shape[1], ctypes.c_float(x["scale"]),
+        ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(lse.data_ptr()),
+        ctypes.c_void_p(status.data_ptr()), ctypes.c_void_p(stream))
+
+
+def test_noalloc_matches_mla_decode_on_two_calls_in_a_row():
+    assert torch.cuda.is_available()
+    import mla_latent_cache_decode_gb300 as mla
+    lib = mla.get_lib()
+    cases = [_inputs([2, 18, 65, 201, 4096, 1], 16, 31, "sharp"),
+             _inputs([9000, 7, 300, 1200, 64, 129, 1, 3333], 64, 32, "normal")]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    results = []
+    for x in cases:   # two calls in a row, different batch and lengths
+        out = torch.full((x["B"], 128, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((x["B"], 128), float("nan"), dtype=torch.float32, device="cuda")
+        rc = _noalloc_via_c_abi(lib, x, out, lse, status)
+        assert rc == 0, mla.get_lib().mla_last_error_detail()
+        results.append((out, lse))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for x, (out, lse) in zip(cases, results):
+        ref = torch.empty((x["B"], 128, 512), dtype=torch.bfloat16, device="cuda")
+        ref_lse = torch.empty((x["B"], 128), dtype=torch.float32, device="cuda")
+        mla.mla_decode(x["q"], x["cache"], x["bt"], x["sl"], x["scale"], ref, ref_lse)
+        torch.cuda.synchronize()
+        assert_close(host_f64(out), host_f64(ref), "noalloc vs mla_decode")
+        assert_lse_close(lse.cpu().numpy(), ref_lse.cpu().numpy())
+
+
+def test_noalloc_rejects_batch_beyond_its_scratch():
+    import mla_latent_cache_decode_gb300 as mla
+    lib = mla.get_lib()
+    rc = lib.mla_decode_noalloc(None, None, 1, 64, None, 1, None, 8193, 128, 64,
+                                ctypes.c_float(0.1), None, None, None, None)
+    assert rc == 1
+    assert b"MLA_NOALLOC_MAX_BATCH" in lib.mla_last_error_detail()
