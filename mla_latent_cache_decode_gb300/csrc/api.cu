@@ -21,6 +21,12 @@ cudaError_t launch_plan_combine(void *ws, int32_t batch, int32_t heads, int32_t 
 cudaError_t launch_offsets_combine(const float *o_part, const float *lse_part,
                                    const int32_t *offsets, int32_t batch, int32_t heads, void *out,
                                    float *lse, cudaStream_t stream);
+int tc_unit_tokens();
+int tc_max_pairs();
+cudaError_t launch_decode_tc(const void *q, const void *cache, int64_t num_blocks, int32_t block_size,
+                             const int32_t *block_table, int32_t max_blocks_per_seq, int32_t batch,
+                             float softmax_scale, void *out, float *lse, void *ws,
+                             int32_t max_ranges, int32_t *dev_status, cudaStream_t stream);
 int simt_unit_tokens();
 cudaError_t launch_decode_simt(const void *q, const void *cache, int64_t num_blocks,
                                int32_t block_size, const int32_t *block_table,
@@ -64,8 +70,8 @@ int sm_count_current(int *out_dev) {
   return counts[dev];
 }
 
-// Ranges of the plan: one per SM.
-int max_ranges_current() { return sm_count_current(nullptr); }
+// Ranges of the plan: one per co-resident CTA pair of the tensor-core kernel.
+int max_ranges_current() { return tc_max_pairs(); }
 
 bool block_size_ok(int32_t bs) { return bs == 16 || bs == 32 || bs == 64 || bs == 128 || bs == 256; }
 
@@ -175,7 +181,7 @@ mla_status_t mla_decode_plan(const int32_t *seq_lens, int32_t batch, int32_t num
   if (need == 0) return fail(MLA_ERR_CUDA, "cannot query the current device");
   if (workspace_bytes < need)
     return fail(MLA_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu", workspace_bytes, need);
-  cudaError_t e = launch_plan(seq_lens, batch, simt_unit_tokens(), max_blocks_per_seq,
+  cudaError_t e = launch_plan(seq_lens, batch, tc_unit_tokens(), max_blocks_per_seq,
                               block_size, max_ranges_current(), workspace, num_heads, dev_status,
                               (cudaStream_t)stream);
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "plan launch");
@@ -194,9 +200,9 @@ mla_status_t mla_decode_planned(const void *q, const void *cache, int64_t num_bl
   if (s != MLA_OK || batch == 0) return s;
   const int ranges = max_ranges_current();
   cudaStream_t st = (cudaStream_t)stream;
-  cudaError_t e = launch_decode_simt(q, cache, num_blocks, block_size, block_table,
-                                     max_blocks_per_seq, batch, softmax_scale, out, lse, workspace,
-                                     ranges, dev_status, st);
+  cudaError_t e = launch_decode_tc(q, cache, num_blocks, block_size, block_table,
+                                   max_blocks_per_seq, batch, softmax_scale, out, lse, workspace,
+                                   ranges, dev_status, st);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   e = launch_plan_combine(workspace, batch, num_heads, ranges, out, lse, st);
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "combine launch");

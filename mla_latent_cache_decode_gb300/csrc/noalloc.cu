@@ -12,12 +12,12 @@ cudaError_t launch_plan(const int32_t *seq_lens, int32_t batch, int32_t unit_tok
                         void *ws, int32_t heads, int32_t *dev_status, cudaStream_t stream);
 cudaError_t launch_plan_combine(void *ws, int32_t batch, int32_t heads, int32_t max_ranges,
                                 void *out, float *lse, cudaStream_t stream);
-int simt_unit_tokens();
-cudaError_t launch_decode_simt(const void *q, const void *cache, int64_t num_blocks,
-                               int32_t block_size, const int32_t *block_table,
-                               int32_t max_blocks_per_seq, int32_t batch, float softmax_scale,
-                               void *out, float *lse, void *ws, int32_t max_ranges,
-                               int32_t *dev_status, cudaStream_t stream);
+int tc_unit_tokens();
+int tc_max_pairs();
+cudaError_t launch_decode_tc(const void *q, const void *cache, int64_t num_blocks, int32_t block_size,
+                             const int32_t *block_table, int32_t max_blocks_per_seq, int32_t batch,
+                             float softmax_scale, void *out, float *lse, void *ws,
+                             int32_t max_ranges, int32_t *dev_status, cudaStream_t stream);
 mla_status_t noalloc_fail(mla_status_t s, const char *msg);
 }  // namespace mla
 
@@ -52,13 +52,6 @@ void *scratch_address(int *err) {
   return addr[dev];
 }
 
-int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-  return n;
-}
-
 }  // namespace
 
 using namespace mla;
@@ -79,10 +72,11 @@ extern "C" mla_status_t mla_decode_noalloc(const void *q, const void *cache, int
                                                       : MLA_ERR_UNSUPPORTED,
                         "batch >= 0, num_heads == 128 and block_size > 0 are required");
   if (batch == 0) return MLA_OK;
-  // Ranges of the split plan: one per SM, as many as the fixed scratch holds.
-  const int sms = sm_count();
-  if (sms <= 0) return noalloc_fail(MLA_ERR_CUDA, "cannot query the current device");
-  int ranges = sms;
+  // Ranges of the split plan: one per co-resident CTA pair, as many as the
+  // fixed scratch holds.
+  const int pairs = tc_max_pairs();
+  if (pairs <= 0) return noalloc_fail(MLA_ERR_CUDA, "cannot query the current device");
+  int ranges = pairs;
   while (ranges > 1 && workspace_layout(batch, kHeads, ranges).total > MLA_NOALLOC_SCRATCH_BYTES)
     --ranges;
   if (workspace_layout(batch, kHeads, ranges).total > MLA_NOALLOC_SCRATCH_BYTES)
@@ -106,11 +100,11 @@ extern "C" mla_status_t mla_decode_noalloc(const void *q, const void *cache, int
   void *ws = scratch_address(&err);
   if (!ws) return noalloc_fail(MLA_ERR_CUDA, "cudaGetSymbolAddress of the scratch array failed");
   cudaStream_t st = (cudaStream_t)stream;
-  cudaError_t e = launch_plan(seq_lens, batch, simt_unit_tokens(), max_blocks_per_seq, block_size,
+  cudaError_t e = launch_plan(seq_lens, batch, tc_unit_tokens(), max_blocks_per_seq, block_size,
                               ranges, ws, num_heads, dev_status, st);
   if (e == cudaSuccess)
-    e = launch_decode_simt(q, cache, num_blocks, block_size, block_table, max_blocks_per_seq,
-                           batch, softmax_scale, out, lse, ws, ranges, dev_status, st);
+    e = launch_decode_tc(q, cache, num_blocks, block_size, block_table, max_blocks_per_seq, batch,
+                         softmax_scale, out, lse, ws, ranges, dev_status, st);
   if (e == cudaSuccess) e = launch_plan_combine(ws, batch, num_heads, ranges, out, lse, st);
   if (e != cudaSuccess) return noalloc_fail(MLA_ERR_CUDA, cudaGetErrorString(e));
   return MLA_OK;
