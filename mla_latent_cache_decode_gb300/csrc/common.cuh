@@ -6,7 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/mla.h"
+#include "mla.h"
 
 namespace mla {
 

@@ -6,29 +6,37 @@
 // 512-dim kv_c  [dp-attention-expert-parallel-mla-kv-replication
 // (inferenceinterviews.com), "A strong answer"; MLA 的 TP 切分 (10100.com),
 // sections 2.2 and 3.1; DP 与 DPA 的区别 (chengxuchu.com), v_head_dim =
-// kv_lora_rank].  Because all 128 heads read the same row, the step is a dense
+// kv_lora_rank].  All 128 heads read the same row, so the step is a dense
 // contraction: S = Q K^T is [128 x 576] x [576 x tokens] and O = P V is
-// [128 x tokens] x [tokens x 512], run on the tensor cores.
+// [128 x tokens] x [tokens x 512], run on the tensor cores (M = 128 heads).
 //
-// How (one CTA pair = one cluster per split range of the plan):
-//   - The pair splits the OUTPUT dims: CTA r owns O[:, 256r .. 256r+255] in
-//     tensor memory (256 fp32 columns) and loads only the columns it needs of
-//     every cache row: kv_c [256r, 256r+256) and rope [512+32r, 512+32r+32),
-//     288 of the 576 dims.  No byte of the cache is loaded twice.
-//   - Each CTA computes the partial score over its 288 dims, S_r = Q_r K_r^T
-//     (M = 128 heads, N = 64 tokens, K = 288), sends it to the peer with
-//     st.async into the peer's shared memory, and adds the peer's partial:
-//     both CTAs then hold the same full S (fp32 addition commutes) and take
-//     identical softmax decisions.
-//   - Q_r (128 x 288 bf16) and P (128 x 64 bf16) live in tensor memory as the
-//     A operand, so the tensor core reads only the cache tile from shared
-//     memory (64 B/clk at full rate).
-//   - Warp roles: warp 0 issues TMA loads of paged tiles through a 4-stage
-//     mbarrier ring; warp 1 issues the MMAs; warps 2-5 (one thread per head)
-//     run the exchange, an online softmax with lazy rescaling of O, and the
-//     epilogue.
-//   - Split-KV: a request spanning several plan ranges leaves fp32 partials
-//     (normalised O and its log-sum-exp), merged by the combine kernel.
+// Layout of the work.  The fp32 output of one request, 128 heads x 512 dims,
+// is exactly one SM's tensor memory, which would leave no room for S.  So two
+// CTAs share a split range of the plan and split the OUTPUT dims: CTA r owns
+// O[:, 256r .. 256r+255].  Each CTA computes the full score S itself (the QK
+// contraction is done by both CTAs: moving partial scores between SMs costs
+// more than recomputing them), then P V for its half.  Both CTAs read the same
+// tiles at about the same time, so the second read is served by L2.
+//
+// Operands.  Q's 256 "own" kv_c dims live in tensor memory (A operand); its
+// other 256 dims and its 64 rope dims live in shared memory (A operand from a
+// shared-memory descriptor).  S is double-buffered in tensor memory, so the S
+// MMAs of the next tile run while the softmax works on this one; P (bf16) is
+// written over the S buffer it came from and read from there by P V.  A 64-token cache tile arrives by TMA in two large boxes,
+// 128-byte swizzled: the "other" part (the other 256 kv_c dims + 64 rope dims)
+// and the "own" part (this CTA's 256 value dims).  S is accumulated over the
+// other dims first, then rope, then the own dims, so the other part of a slot
+// is released early and refilled 1.5 tiles ahead, while the own part (also the
+// V operand of P V) is held until P V and is needed only at the end of the
+// next-but-one S: two slots per part hide the load latency.  Upcoming tiles
+// are prefetched into L2 so that refills are served by L2.
+//
+// Warp roles: warp 0 loads the own parts (and prefetches into L2); warp 3
+// loads Q's other half per segment and the other parts; warp 1 issues the S
+// MMAs (and owns the tensor memory allocation); warp 2 issues the P V MMAs;
+// warps 4-7 (one thread per head) load Q into tensor memory, run the online
+// softmax with lazy rescaling of O, and write the output (or split partials
+// plus log-sum-exp).
 #include "common.cuh"
 #include "sm100.cuh"
 
@@ -37,32 +45,38 @@ namespace tc {
 
 using namespace sm100;
 
-constexpr int kTile = 64;                 // tokens per tile (= plan unit)
-constexpr int kStages = 4;
-constexpr int kVHalf = 256;               // output dims per CTA
-constexpr int kRopeHalf = 32;             // rope dims per CTA
-constexpr int kRegionBytes = kTile * 128; // one 64-dim SW128 region of a tile: 8 KB
-constexpr int kRopeBytes = kTile * 64;    // the 32-dim SW64 rope region: 4 KB
-constexpr int kStageBytes = 4 * kRegionBytes + kRopeBytes;  // 36 KB
-constexpr int kRecvStride = kTile + 4;    // floats per received row (16 B pad)
-constexpr int kThreads = 192;             // 6 warps
+constexpr int kTile = 64;                  // tokens per tile (= plan unit)
+constexpr int kSlots = 2;                  // slots per part
+constexpr int kVHalf = 256;                // output dims per CTA
+constexpr int kChunkBytes = kTile * 128;   // one 64-dim, 64-token SW128 chunk: 8 KB
+constexpr int kQChunkBytes = 128 * 128;    // one 64-dim chunk of Q for 128 heads: 16 KB
+constexpr int kThreads = 256;              // 8 warps
 constexpr int kSoftmaxThreads = 128;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQ = 352;
+constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;  // S buffers at kColS + 64 * (g & 1)
 constexpr uint64_t kWaitBudgetNs = 100000000ull;  // 100 ms per wait, far above any legal wait
 constexpr uint64_t kDrainBudgetNs = 10000000ull;  // 10 ms to drain in-flight copies on abort
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
+constexpr int kPrefetchTiles = 4;                 // tiles prefetched into L2 ahead of the loads
 
 struct __align__(1024) Smem {
-  uint8_t stage[kStages][kStageBytes];
-  float recv[2][kSoftmaxThreads][kRecvStride];
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  uint64_t s_full, s_free, p_full, pv_done, q_ready, fin;
-  uint64_t recv_full[2];
-  uint64_t send_ok[2];
+  uint8_t q_other[4][kQChunkBytes];      // Q[:, other 256 dims], 4 chunks of 64 dims: 64 KB
+  uint8_t q_rope[kQChunkBytes];          // Q[:, 64 rope dims]: 16 KB
+  uint8_t other[kSlots][5][kChunkBytes]; // other 256 kv_c dims (4 chunks) + rope: 40 KB / slot
+  uint8_t own[kSlots][4][kChunkBytes];   // own 256 value dims: 32 KB / slot
+  uint64_t other_full[kSlots], other_empty[kSlots], own_full[kSlots], own_empty[kSlots];
+  uint64_t s_full[2], pv_done[2];  // per S buffer: S ready / P V of that buffer's tile done
+  uint64_t p_full, q_full, q_tmem, q_free, fin_qk, fin_pv;
   uint32_t tmem_base;
   int abort;
+};
+
+// Tensor maps over the cache viewed as [rows = NB*BS][576]: 3-D views
+// {64 columns, rows, 9 chunks} (chunk stride 128 B) fetch several 64-dim
+// chunks of 64 rows in one box, laid out chunk after chunk; the 2-D view
+// serves pages shorter than a tile.
+struct Maps {
+  CUtensorMap kv5, kv4, kv1, kv9, kv2d, q;
 };
 
 struct Params {
@@ -80,7 +94,7 @@ struct Params {
   int32_t *dev_status;
 };
 
-// Segment of range p: request b, tokens [t0, t1).  Iterates in plan order.
+// Segments of range p, in plan order: request b, tokens [t0, t1).
 struct SegIter {
   PlanView v;
   int32_t batch, U, P, r0, r1, b;
@@ -114,12 +128,10 @@ __device__ __forceinline__ void set_abort(Smem &s, int32_t *dev_status) {
   report(dev_status, MLA_ERR_DEVICE_TIMEOUT);
 }
 
-// Every lane polls (each gets the barrier's acquire), then the warp agrees:
-// the warp proceeds only if every lane saw the phase complete, so control flow
-// around warp-collective tcgen05 instructions stays uniform.
-template <bool kCluster = false>
+// Every lane polls (each gets the barrier's acquire), then the warp agrees, so
+// control flow around warp-collective tcgen05 instructions stays uniform.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const volatile int *abort) {
-  const bool ok = mbar_wait<kCluster>(bar, parity, abort, kWaitBudgetNs);
+  const bool ok = mbar_wait(bar, parity, abort, kWaitBudgetNs);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -128,36 +140,58 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap map_v,
-                     const __grid_constant__ CUtensorMap map_r, const Params prm) {
+// Rows of one tile: the cache row of each page-sized (or tile-sized) box.
+struct TileRows {
+  int boxes;
+  int32_t y[kTile / 16];
+};
+
+__device__ __forceinline__ TileRows tile_rows(const int32_t *table, int32_t tt, int n, int BS,
+                                              int box_rows, int64_t nb, int32_t *dev_status,
+                                              bool report_bad) {
+  TileRows r;
+  r.boxes = (n + box_rows - 1) / box_rows;
+  for (int j = 0; j < r.boxes; ++j) {
+    const int32_t tok = tt + j * box_rows;
+    int32_t blk = table[tok / BS];
+    if (blk < 0 || blk >= nb) {
+      if (report_bad) report(dev_status, MLA_ERR_DEVICE_RANGE);
+      blk = 0;
+    }
+    r.y[j] = blk * BS + (tok % BS);
+  }
+  return r;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ Maps maps, const Params prm) {
   extern __shared__ uint8_t smem_raw[];
   Smem &s = *reinterpret_cast<Smem *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
+  const int half = blockIdx.x & 1;  // this CTA owns output dims [256*half, 256*half + 256)
   const int pair = blockIdx.x >> 1;
   const PlanView v = plan_view(prm.ws, prm.batch, kHeads, prm.max_ranges);
   const volatile int *abort_flag = &s.abort;
 
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(smem_u32(&s.full[i]), 1);
-      mbar_init(smem_u32(&s.empty[i]), 1);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(smem_u32(&s.other_full[i]), 1);
+      mbar_init(smem_u32(&s.other_empty[i]), 1);
+      mbar_init(smem_u32(&s.own_full[i]), 1);
+      mbar_init(smem_u32(&s.own_empty[i]), 1);
     }
-    mbar_init(smem_u32(&s.s_full), 1);
-    mbar_init(smem_u32(&s.s_free), kSoftmaxThreads);
-    mbar_init(smem_u32(&s.p_full), kSoftmaxThreads);
-    mbar_init(smem_u32(&s.pv_done), 1);
-    mbar_init(smem_u32(&s.q_ready), kSoftmaxThreads);
-    mbar_init(smem_u32(&s.fin), 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&s.recv_full[i]), 1);
-      mbar_init(smem_u32(&s.send_ok[i]), kSoftmaxThreads / 32);  // one arrival per peer warp
+      mbar_init(smem_u32(&s.s_full[i]), 1);
+      mbar_init(smem_u32(&s.pv_done[i]), 1);
     }
+    mbar_init(smem_u32(&s.p_full), kSoftmaxThreads);
+    mbar_init(smem_u32(&s.q_full), 1);
+    mbar_init(smem_u32(&s.q_tmem), kSoftmaxThreads);
+    mbar_init(smem_u32(&s.q_free), 1);
+    mbar_init(smem_u32(&s.fin_qk), 1);
+    mbar_init(smem_u32(&s.fin_pv), 1);
     s.abort = 0;
     fence_mbarrier_init_cluster();
-    prefetch_tmap(&map_v);
-    prefetch_tmap(&map_r);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&s.tmem_base), kTmemCols);
@@ -165,315 +199,365 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // barriers of both CTAs initialised before any remote access
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
 
   const int32_t P = v.hdr->num_ranges;
   const bool active = pair < P;
+  const int own0 = half * 4;        // first own 64-dim chunk (of the 8 kv_c chunks)
+  const int oth0 = (1 - half) * 4;  // first other chunk
+  const int BS = prm.block_size;
+  const bool big_pages = BS >= kTile;  // a tile lies inside one page: one box per part
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp == 0 || warp == 3) {
+    // ------------------------------------------------------------ TMA producers
     if (active && elect_one_sync()) {
+      const bool own_role = (warp == 0);
       const uint64_t policy = policy_evict_first();
       SegIter it;
       it.init(v, prm.batch, pair);
       int32_t t0, t1, Ub;
       bool split;
-      int stage = 0;
-      uint32_t phase = 0;
-      const int BS = prm.block_size;
+      uint32_t g = 0, seg = 0;
       const int box_rows = BS < kTile ? BS : kTile;
+      const uint32_t box_bytes = (uint32_t)(box_rows * 128);
       const int64_t nb = prm.num_blocks;
+      // a second cursor walks the same tiles kPrefetchTiles ahead and asks L2
+      // for them (the own-part producer only)
+      SegIter pf;
+      pf.init(v, prm.batch, pair);
+      int32_t pf_t = 0, pf_t1 = 0, pf_Ub;
+      bool pf_split, pf_more = own_role;
+      auto prefetch_one = [&]() {
+        while (pf_more && pf_t >= pf_t1) pf_more = pf.next(pf_t, pf_t1, pf_split, pf_Ub);
+        if (!pf_more) return;
+        const int32_t *tab = prm.block_table + (int64_t)pf.b * prm.max_blocks_per_seq;
+        const TileRows r = tile_rows(tab, pf_t, min(kTile, pf_t1 - pf_t), BS, box_rows, nb,
+                                     prm.dev_status, false);
+        for (int j = 0; j < r.boxes; ++j) {
+          if (big_pages) {
+            tma_prefetch_3d(&maps.kv9, 0, r.y[j], 0);
+          } else {
+            for (int c = 0; c < 9; ++c) tma_prefetch_2d(&maps.kv2d, 64 * c, r.y[j]);
+          }
+        }
+        pf_t += kTile;
+      };
+      if (own_role) {
+        prefetch_tmap(&maps.kv4);
+        prefetch_tmap(&maps.kv9);
+        for (int i = 0; i < kPrefetchTiles; ++i) prefetch_one();
+      } else {
+        prefetch_tmap(&maps.kv5);
+        prefetch_tmap(&maps.kv1);
+        prefetch_tmap(&maps.q);
+      }
       bool ok = true;
-      uint32_t issued = 0;
       while (ok && it.next(t0, t1, split, Ub)) {
-        const int32_t *table = prm.block_table + (int64_t)it.b * prm.max_blocks_per_seq;
-        for (int32_t tt = t0; tt < t1 && ok; tt += kTile) {
-          const int n = min(kTile, t1 - tt);
-          if (!mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, abort_flag, kWaitBudgetNs)) {
+        if (!own_role) {
+          // Q[:, other 256 dims] of request b into shared memory
+          if (!mbar_wait(smem_u32(&s.q_free), (seg & 1u) ^ 1u, abort_flag, kWaitBudgetNs)) {
             set_abort(s, prm.dev_status);
-            ok = false;
             break;
           }
-          const int boxes = (n + box_rows - 1) / box_rows;
-          const uint32_t full = smem_u32(&s.full[stage]);
-          mbar_arrive_expect_tx(full, (uint32_t)(boxes * box_rows * (4 * 128 + 64)));
-          const uint32_t base = smem_u32(s.stage[stage]);
-          for (int j = 0; j < boxes; ++j) {
-            const int32_t tok = tt + j * box_rows;
-            int32_t blk = table[tok / BS];
-            if (blk < 0 || blk >= nb) {
-              report(prm.dev_status, MLA_ERR_DEVICE_RANGE);
-              blk = 0;
+          mbar_arrive_expect_tx(smem_u32(&s.q_full), 5 * kQChunkBytes);
+          for (int c = 0; c < 4; ++c)
+            tma_load_2d(smem_u32(s.q_other[c]), &maps.q, 64 * (oth0 + c), it.b * kHeads,
+                        smem_u32(&s.q_full));
+          tma_load_2d(smem_u32(s.q_rope), &maps.q, 512, it.b * kHeads, smem_u32(&s.q_full));
+        }
+        ++seg;
+        const int32_t *table = prm.block_table + (int64_t)it.b * prm.max_blocks_per_seq;
+        for (int32_t tt = t0; tt < t1; tt += kTile, ++g) {
+          if (own_role) prefetch_one();
+          const TileRows r = tile_rows(table, tt, min(kTile, t1 - tt), BS, box_rows, nb,
+                                       prm.dev_status, own_role);
+          const int slot = g % kSlots;
+          const uint32_t par = ((g / kSlots) & 1u) ^ 1u;
+          if (own_role) {
+            if (!mbar_wait(smem_u32(&s.own_empty[slot]), par, abort_flag, kWaitBudgetNs)) {
+              set_abort(s, prm.dev_status);
+              ok = false;
+              break;
             }
-            const int32_t y = blk * BS + (tok % BS);
-            for (int c = 0; c < 4; ++c)
-              tma_load_2d_hint(base + c * kRegionBytes + j * box_rows * 128, &map_v,
-                               (int)rank * kVHalf + 64 * c, y, full, policy);
-            tma_load_2d_hint(base + 4 * kRegionBytes + j * box_rows * 64, &map_r,
-                             512 + (int)rank * kRopeHalf, y, full, policy);
-          }
-          ++issued;
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
+            const uint32_t bar = smem_u32(&s.own_full[slot]);
+            mbar_arrive_expect_tx(bar, 4u * r.boxes * box_bytes);
+            if (big_pages) {
+              tma_load_3d_hint(smem_u32(s.own[slot][0]), &maps.kv4, 0, r.y[0], own0, bar, policy);
+            } else {
+              for (int j = 0; j < r.boxes; ++j)
+                for (int c = 0; c < 4; ++c)
+                  tma_load_2d_hint(smem_u32(s.own[slot][c]) + j * box_bytes, &maps.kv2d,
+                                   64 * (own0 + c), r.y[j], bar, policy);
+            }
+          } else {
+            if (!mbar_wait(smem_u32(&s.other_empty[slot]), par, abort_flag, kWaitBudgetNs)) {
+              set_abort(s, prm.dev_status);
+              ok = false;
+              break;
+            }
+            const uint32_t bar = smem_u32(&s.other_full[slot]);
+            mbar_arrive_expect_tx(bar, 5u * r.boxes * box_bytes);
+            if (big_pages) {
+              if (half == 0) {  // other = chunks 4..7, rope = chunk 8: contiguous
+                tma_load_3d_hint(smem_u32(s.other[slot][0]), &maps.kv5, 0, r.y[0], 4, bar, policy);
+              } else {          // other = chunks 0..3, then rope
+                tma_load_3d_hint(smem_u32(s.other[slot][0]), &maps.kv4, 0, r.y[0], 0, bar, policy);
+                tma_load_3d_hint(smem_u32(s.other[slot][4]), &maps.kv1, 0, r.y[0], 8, bar, policy);
+              }
+            } else {
+              for (int j = 0; j < r.boxes; ++j)
+                for (int c = 0; c < 5; ++c)
+                  tma_load_2d_hint(smem_u32(s.other[slot][c]) + j * box_bytes, &maps.kv2d,
+                                   c < 4 ? 64 * (oth0 + c) : 512, r.y[j], bar, policy);
+            }
           }
         }
       }
       if (s.abort) {
-        // the consumer gave up: let the last (up to kStages) issued loads land
-        // before this CTA's shared memory can be released
-        for (uint32_t k = 1; k <= (issued < kStages ? issued : (uint32_t)kStages); ++k) {
-          const uint32_t g = issued - k;
-          (void)mbar_wait(smem_u32(&s.full[g % kStages]), (g / kStages) & 1u, nullptr,
+        // the consumers gave up: let the last issued loads land before exit
+        for (int i = 0; i < kSlots; ++i)
+          (void)mbar_wait(smem_u32(own_role ? &s.own_full[i] : &s.other_full[i]), 0, nullptr,
                           kDrainBudgetNs);
-        }
+        if (!own_role) (void)mbar_wait(smem_u32(&s.q_full), 0, nullptr, kDrainBudgetNs);
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S = Q K^T issuer
     if (active && elect_one_sync()) {
       SegIter it;
       it.init(v, prm.batch, pair);
       int32_t t0, t1, Ub;
       bool split;
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t q_ph = 0, s_free_ph = 0, p_full_ph = 0;
-      uint32_t qk_issued = 0;
-      const uint32_t id_qk = idesc_bf16_f32(128, kTile, 0);
-      const uint32_t id_pv = idesc_bf16_f32(128, kVHalf, 1);
+      uint32_t g = 0, seg = 0;
+      const uint32_t id = idesc_bf16_f32(128, kTile, 0);
+      // descriptors of slot 0 / chunk 0; chunks, slots and k-steps add their
+      // byte offset >> 4 to the 14-bit start-address field (no carry: every
+      // shared-memory address here is below 2^18)
+      const uint64_t d_own = smem_desc(smem_u32(s.own[0][0]), 16, 1024, kSwizzle128B);
+      const uint64_t d_oth = smem_desc(smem_u32(s.other[0][0]), 16, 1024, kSwizzle128B);
+      const uint64_t d_q = smem_desc(smem_u32(s.q_other[0]), 16, 1024, kSwizzle128B);
+      const uint64_t d_rope = smem_desc(smem_u32(s.q_rope), 16, 1024, kSwizzle128B);
+      const uint32_t a_q = tmem + kColQ;
       bool ok = true;
       while (ok && it.next(t0, t1, split, Ub)) {
-        if (!mbar_wait(smem_u32(&s.q_ready), q_ph, abort_flag, kWaitBudgetNs)) {
+        if (!mbar_wait(smem_u32(&s.q_full), seg & 1u, abort_flag, kWaitBudgetNs) ||
+            !mbar_wait(smem_u32(&s.q_tmem), seg & 1u, abort_flag, kWaitBudgetNs)) {
           set_abort(s, prm.dev_status);
           break;
         }
-        q_ph ^= 1u;
+        ++seg;
         tc_fence_after();
-        const int ntiles = (t1 - t0 + kTile - 1) / kTile;
-        int prev_stage = 0, prev_n = 0;
-        for (int i = 0; i <= ntiles && ok; ++i) {
-          if (i < ntiles) {
-            // ---- S = Q_r K_r^T for tile i
-            if (!mbar_wait(smem_u32(&s.full[stage]), phase, abort_flag, kWaitBudgetNs)) {
-              set_abort(s, prm.dev_status);
-              ok = false;
-              break;
-            }
-            if (qk_issued > 0) {
-              if (!mbar_wait(smem_u32(&s.s_free), s_free_ph, abort_flag, kWaitBudgetNs)) {
-                set_abort(s, prm.dev_status);
-                ok = false;
-                break;
-              }
-              s_free_ph ^= 1u;
-            }
-            tc_fence_after();
-            const uint32_t base = smem_u32(s.stage[stage]);
-            for (int c = 0; c < 4; ++c)
-              for (int kk = 0; kk < 4; ++kk)
-                mma_ts(tmem + kColS, tmem + kColQ + c * 32 + kk * 8,
-                       smem_desc(base + c * kRegionBytes + kk * 32, 16, 1024, kSwizzle128B), id_qk,
-                       (c | kk) != 0);
-            for (int kk = 0; kk < 2; ++kk)
-              mma_ts(tmem + kColS, tmem + kColQ + 128 + kk * 8,
-                     smem_desc(base + 4 * kRegionBytes + kk * 32, 16, 512, kSwizzle64B), id_qk, 1);
-            mma_commit(smem_u32(&s.s_full));
-            ++qk_issued;
+        for (int32_t tt = t0; tt < t1; tt += kTile, ++g) {
+          const int slot = g % kSlots;
+          const uint32_t par = (g / kSlots) & 1u;
+          const uint32_t d_s = tmem + kColS + 64 * (g & 1u);
+          // the S buffer is free once P V of tile g-2 (which read P from it) is done
+          if (!mbar_wait(smem_u32(&s.other_full[slot]), par, abort_flag, kWaitBudgetNs) ||
+              (g >= 2 && !mbar_wait(smem_u32(&s.pv_done[g & 1u]), ((g >> 1) - 1) & 1u, abort_flag,
+                                    kWaitBudgetNs))) {
+            set_abort(s, prm.dev_status);
+            ok = false;
+            break;
           }
-          if (i > 0) {
-            // ---- O += P V for tile i-1
-            if (!mbar_wait(smem_u32(&s.p_full), p_full_ph, abort_flag, kWaitBudgetNs)) {
-              set_abort(s, prm.dev_status);
-              ok = false;
-              break;
-            }
-            p_full_ph ^= 1u;
-            tc_fence_after();
-            const uint32_t base = smem_u32(s.stage[prev_stage]);
-            const int ksteps = (prev_n + 15) / 16;
-            for (int kt = 0; kt < ksteps; ++kt)
-              mma_ts(tmem + kColO, tmem + kColP + kt * 8,
-                     smem_desc(base + kt * 2048, kRegionBytes, 1024, kSwizzle128B), id_pv,
-                     (i > 1 || kt > 0) ? 1u : 0u);
-            mma_commit(smem_u32(&s.pv_done));
-            mma_commit(smem_u32(&s.empty[prev_stage]));
-          }
-          if (i < ntiles) {
-            prev_stage = stage;
-            prev_n = min(kTile, t1 - (t0 + i * kTile));
-            if (++stage == kStages) {
-              stage = 0;
-              phase ^= 1u;
+          tc_fence_after();
+          // other 256 kv_c dims, then rope: A = Q (shared memory), B = other part
+          const uint64_t bo = d_oth + (uint64_t)((slot * 5 * kChunkBytes) >> 4);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t a = d_q + (uint64_t)((c * kQChunkBytes + kk * 32) >> 4);
+              const uint64_t b = bo + (uint64_t)((c * kChunkBytes + kk * 32) >> 4);
+              if (c == 0 && kk == 0) mma_ss(d_s, a, b, id, 0); else mma_ss_acc(d_s, a, b, id);
             }
           }
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss_acc(d_s, d_rope + (uint64_t)((kk * 32) >> 4),
+                       bo + (uint64_t)((4 * kChunkBytes + kk * 32) >> 4), id);
+          mma_commit(smem_u32(&s.other_empty[slot]));
+          // own 256 kv_c dims: A = Q (tensor memory), B = own part
+          if (!mbar_wait(smem_u32(&s.own_full[slot]), par, abort_flag, kWaitBudgetNs)) {
+            set_abort(s, prm.dev_status);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t bw = d_own + (uint64_t)((slot * 4 * kChunkBytes) >> 4);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts_acc(d_s, a_q + c * 32 + kk * 8,
+                         bw + (uint64_t)((c * kChunkBytes + kk * 32) >> 4), id);
+          }
+          mma_commit(smem_u32(&s.s_full[g & 1u]));
         }
+        if (!ok) break;
+        mma_commit(smem_u32(&s.q_free));  // Q of this segment no longer read
       }
-      // all issued MMAs complete before teardown (not cut short by the abort flag)
-      mma_commit(smem_u32(&s.fin));
-      if (!mbar_wait(smem_u32(&s.fin), 0, nullptr, kWaitBudgetNs)) report(prm.dev_status, MLA_ERR_DEVICE_TIMEOUT);
+      mma_commit(smem_u32(&s.fin_qk));
+      if (!mbar_wait(smem_u32(&s.fin_qk), 0, nullptr, kWaitBudgetNs))
+        report(prm.dev_status, MLA_ERR_DEVICE_TIMEOUT);
     }
-  } else {
-    // ------------------------------------------------------------ softmax / exchange / epilogue
-    const int q4 = warp & 3;                  // TMEM lane quadrant of this warp
-    const int h = q4 * 32 + lane;             // head = TMEM lane
-    const uint32_t lane_addr = tmem + ((uint32_t)(q4 * 32) << 16);
-    const int st = tid - 64;                  // 0..127 within the softmax group
-
-    // requests with no context: out = 0 (this CTA's half), lse = -inf
-    for (int b = pair; b < prm.batch; b += (int)(gridDim.x >> 1)) {
-      if (v.seq_len[b] != 0) continue;
-      uint4 *o = (uint4 *)(prm.out + ((int64_t)b * kHeads + h) * kVDim + rank * kVHalf);
-#pragma unroll 4
-      for (int k = 0; k < kVHalf / 8; ++k) o[k] = make_uint4(0, 0, 0, 0);
-      if (prm.lse && rank == 0) prm.lse[(int64_t)b * kHeads + h] = -INFINITY;
-    }
-
-    if (active) {
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ O += P V issuer
+    if (active && elect_one_sync()) {
       SegIter it;
       it.init(v, prm.batch, pair);
       int32_t t0, t1, Ub;
       bool split;
-      uint32_t s_full_ph = 0, pv_ph = 0;
-      uint32_t xcount = 0;   // score exchanges so far (alternating buffers)
-      uint32_t gtile = 0;    // tiles so far (the smem stage of a tile is gtile % kStages)
-      const uint32_t my_recv[2] = {smem_u32(&s.recv[0][st][0]), smem_u32(&s.recv[1][st][0])};
-      const uint32_t peer_recv[2] = {mapa_shared(my_recv[0], peer), mapa_shared(my_recv[1], peer)};
-      const uint32_t peer_recv_full[2] = {mapa_shared(smem_u32(&s.recv_full[0]), peer),
-                                          mapa_shared(smem_u32(&s.recv_full[1]), peer)};
-      const uint32_t peer_send_ok[2] = {mapa_shared(smem_u32(&s.send_ok[0]), peer),
-                                        mapa_shared(smem_u32(&s.send_ok[1]), peer)};
+      uint32_t g = 0;
+      const uint32_t id_pv = idesc_bf16_f32(128, kVHalf, 1);
+      const uint64_t d_own = smem_desc(smem_u32(s.own[0][0]), kChunkBytes, 1024, kSwizzle128B);
       bool ok = true;
       while (ok && it.next(t0, t1, split, Ub)) {
-        const int b = it.b;
-        // ---- Q_r of request b into tensor memory (A operand): 144 columns
-        {
-          const uint4 *qrow = (const uint4 *)(prm.q + ((int64_t)b * kHeads + h) * kRow);
-          uint4 buf[36];
-#pragma unroll
-          for (int k = 0; k < 32; ++k) buf[k] = __ldg(qrow + rank * 32 + k);        // kv_c half
-#pragma unroll
-          for (int k = 0; k < 4; ++k) buf[32 + k] = __ldg(qrow + 64 + rank * 4 + k);  // rope half
-#pragma unroll
-          for (int c = 0; c < 9; ++c)
-            tmem_st16(lane_addr + kColQ + 16 * c, reinterpret_cast<const uint32_t *>(&buf[4 * c]));
-          tmem_wait_st();
+        for (int32_t tt = t0; tt < t1; tt += kTile, ++g) {
+          const int n = min(kTile, t1 - tt);
+          const int slot = g % kSlots;
+          if (!mbar_wait(smem_u32(&s.p_full), g & 1u, abort_flag, kWaitBudgetNs)) {
+            set_abort(s, prm.dev_status);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t bw = d_own + (uint64_t)((slot * 4 * kChunkBytes) >> 4);
+          const uint32_t a_p = tmem + kColS + 64 * (g & 1u);  // P sits in its S buffer
+          const int ksteps = (n + 15) >> 4;
+          for (int kt = 0; kt < ksteps; ++kt)
+            mma_ts(tmem + kColO, a_p + kt * 8, bw + (uint64_t)((kt * 2048) >> 4), id_pv,
+                   (tt > t0 || kt > 0) ? 1u : 0u);
+          mma_commit(smem_u32(&s.pv_done[g & 1u]));
+          mma_commit(smem_u32(&s.own_empty[slot]));
         }
+      }
+      mma_commit(smem_u32(&s.fin_pv));
+      if (!mbar_wait(smem_u32(&s.fin_pv), 0, nullptr, kWaitBudgetNs))
+        report(prm.dev_status, MLA_ERR_DEVICE_TIMEOUT);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax / epilogue
+    const int q4 = warp & 3;              // TMEM lane quadrant of this warp
+    const int h = q4 * 32 + lane;         // head = TMEM lane
+    const uint32_t lane_addr = tmem + ((uint32_t)(q4 * 32) << 16);
+    const int st = tid - 128;             // 0..127 within the softmax group
+
+    // requests with no context: out = 0 (this CTA's half), lse = -inf
+    for (int b = pair; b < prm.batch; b += (int)(gridDim.x >> 1)) {
+      if (v.seq_len[b] != 0) continue;
+      uint4 *o = (uint4 *)(prm.out + ((int64_t)b * kHeads + h) * kVDim + half * kVHalf);
+#pragma unroll 4
+      for (int k = 0; k < kVHalf / 8; ++k) o[k] = make_uint4(0, 0, 0, 0);
+      if (prm.lse && half == 0) prm.lse[(int64_t)b * kHeads + h] = -INFINITY;
+    }
+
+    if (active) {
+      // Q[h, own 256 dims] of request qb into tensor memory (A operand of S)
+      auto load_q_own = [&](int qb) {
+        const uint4 *qrow = (const uint4 *)(prm.q + ((int64_t)qb * kHeads + h) * kRow);
+        uint4 buf[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) buf[k] = __ldg(qrow + half * 32 + k);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          tmem_st16(lane_addr + kColQ + 16 * c, reinterpret_cast<const uint32_t *>(&buf[4 * c]));
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(smem_u32(&s.q_ready));
+        mbar_arrive(smem_u32(&s.q_tmem));
+      };
+      SegIter it;
+      it.init(v, prm.batch, pair);
+      int32_t t0, t1, Ub;
+      bool split;
+      uint32_t g = 0;  // tiles so far
+      bool ok = true;
+      bool have = it.next(t0, t1, split, Ub);
+      if (have) load_q_own(it.b);
+      while (ok && have) {
+        const int b = it.b;
+        SegIter nx = it;  // the segment after this one, if any
+        int32_t nt0, nt1, nUb;
+        bool nsplit;
+        const bool have_next = nx.next(nt0, nt1, nsplit, nUb);
 
         float m_used = -INFINITY, l = 0.f;
-        const int ntiles = (t1 - t0 + kTile - 1) / kTile;
-        for (int i = 0; i < ntiles; ++i, ++gtile) {
-          const int n = min(kTile, t1 - (t0 + i * kTile));
-          // ---- own partial scores S_r (fp32) out of tensor memory
-          if (!warp_wait(smem_u32(&s.s_full), s_full_ph, abort_flag)) {
+        for (int32_t tt = t0; tt < t1; tt += kTile, ++g) {
+          const int n = min(kTile, t1 - tt);
+          const bool first = (tt == t0), last = (tt + kTile >= t1);
+          const uint32_t buf_col = kColS + 64 * (g & 1u);
+          if (!warp_wait(smem_u32(&s.s_full[g & 1u]), (g >> 1) & 1u, abort_flag)) {
             if (lane == 0) set_abort(s, prm.dev_status);
             ok = false;
             break;
           }
-          s_full_ph ^= 1u;
           tc_fence_after();
           uint32_t xr[kTile];
-          tmem_ld32(lane_addr + kColS, &xr[0]);
-          tmem_ld32(lane_addr + kColS + 32, &xr[32]);
+          tmem_ld32(lane_addr + buf_col, &xr[0]);
+          tmem_ld32(lane_addr + buf_col + 32, &xr[32]);
           tmem_wait_ld();
-          tc_fence_before();
-          mbar_arrive(smem_u32(&s.s_free));
-          // ---- send S_r to the peer, receive S_peer
-          const int xb = xcount & 1;
-          const uint32_t use = xcount >> 1;
-          if (use > 0 && !warp_wait<true>(smem_u32(&s.send_ok[xb]), (use - 1) & 1u, abort_flag)) {
-            if (lane == 0) set_abort(s, prm.dev_status);
-            ok = false;
-            break;
-          }
-#pragma unroll
-          for (int k = 0; k < kTile; k += 4)
-            st_async_v4(peer_recv[xb] + 4 * k, xr[k], xr[k + 1], xr[k + 2], xr[k + 3],
-                        peer_recv_full[xb]);
-          if (st == 0)
-            mbar_arrive_expect_tx(smem_u32(&s.recv_full[xb]),
-                                  kSoftmaxThreads * kTile * (uint32_t)sizeof(float));
-          if (!warp_wait<true>(smem_u32(&s.recv_full[xb]), use & 1u, abort_flag)) {
-            if (lane == 0) set_abort(s, prm.dev_status);
-            ok = false;
-            break;
-          }
+          // ---- online softmax in log2 units, lazy rescale of O (eight
+          // independent partial maxima / sums keep the dependency chains short)
           float x[kTile];
-          {
-            const float4 *pr = reinterpret_cast<const float4 *>(&s.recv[xb][st][0]);
+          float mx[8];
 #pragma unroll
-            for (int k = 0; k < kTile / 4; ++k) {
-              const float4 y = pr[k];
-              x[4 * k] = __uint_as_float(xr[4 * k]) + y.x;
-              x[4 * k + 1] = __uint_as_float(xr[4 * k + 1]) + y.y;
-              x[4 * k + 2] = __uint_as_float(xr[4 * k + 2]) + y.z;
-              x[4 * k + 3] = __uint_as_float(xr[4 * k + 3]) + y.w;
-            }
-          }
-          // this warp's rows of recv[xb] are consumed: the peer may refill them
-          __syncwarp();
-          if (lane == 0) mbar_arrive_remote(peer_send_ok[xb]);
-          ++xcount;
-          // ---- online softmax in log2 units, lazy rescale of O
-          float tmax = -INFINITY;
+          for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
 #pragma unroll
           for (int k = 0; k < kTile; ++k) {
-            x[k] = k < n ? x[k] * prm.scale_log2 : -INFINITY;
-            tmax = fmaxf(tmax, x[k]);
+            x[k] = k < n ? __uint_as_float(xr[k]) * prm.scale_log2 : -INFINITY;
+            mx[k & 7] = fmaxf(mx[k & 7], x[k]);
           }
-          const bool first = (i == 0);
+          const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
           const bool rescale = first || tmax > m_used + kRescaleThreshold;
           float alpha = 1.f;
           if (rescale) {
             const float m_new = first ? tmax : fmaxf(m_used, tmax);
-            alpha = first ? 0.f : exp2f(m_used - m_new);
+            alpha = first ? 0.f : ex2_approx(m_used - m_new);
             m_used = m_new;
           }
           uint32_t pk[kTile / 2];
-          float psum = 0.f;
+          float ps[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) ps[k] = 0.f;
 #pragma unroll
           for (int k = 0; k < kTile; k += 2) {
-            const float p0 = exp2f(x[k] - m_used), p1 = exp2f(x[k + 1] - m_used);
-            psum += p0 + p1;
+            const float p0 = ex2_approx(x[k] - m_used), p1 = ex2_approx(x[k + 1] - m_used);
+            ps[(k >> 1) & 7] += p0 + p1;
             pk[k / 2] = pack_bf16(p0, p1);
           }
+          const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
           l = l * alpha + psum;
-          // ---- P and O may be touched only after the previous PV completed
-          if (!first) {
-            if (!warp_wait(smem_u32(&s.pv_done), pv_ph, abort_flag)) {
+          // ---- O may be rescaled only once the previous P V has completed
+          if (!first && __any_sync(0xffffffffu, rescale)) {
+            if (!warp_wait(smem_u32(&s.pv_done[(g - 1) & 1u]), ((g - 1) >> 1) & 1u, abort_flag)) {
               if (lane == 0) set_abort(s, prm.dev_status);
               ok = false;
               break;
             }
-            pv_ph ^= 1u;
             tc_fence_after();
-            if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-              for (int c = 0; c < kVHalf; c += 32) {
-                uint32_t o[32];
-                tmem_ld32(lane_addr + kColO + c, o);
-                tmem_wait_ld();
+            for (int c = 0; c < kVHalf; c += 32) {
+              uint32_t o[32];
+              tmem_ld32(lane_addr + kColO + c, o);
+              tmem_wait_ld();
 #pragma unroll
-                for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-                tmem_st32(lane_addr + kColO + c, o);
-              }
+              for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+              tmem_st32(lane_addr + kColO + c, o);
             }
           }
-          tmem_st32(lane_addr + kColP, pk);
-          // the PV of a tail tile reads rows [0, ceil16(n)): rows past the
+          // P over the first 32 columns of its own S buffer (S already read)
+          tmem_st32(lane_addr + buf_col, pk);
+          // The P V of a tail tile reads rows [0, ceil16(n)); rows past the
           // sequence end hold whatever the page held (maybe NaN; 0 * NaN = NaN),
-          // so zero them in shared memory (a 128-byte row keeps its 16-byte
-          // chunks inside itself under the 128-byte swizzle)
+          // so zero them (a 128-byte row keeps its 16-byte chunks inside itself
+          // under the 128-byte swizzle).
           if (n & 15) {
-            uint8_t *base = s.stage[gtile % kStages];
+            uint8_t *base = s.own[g % kSlots][0];
             const int rows = ((n + 15) & ~15) - n;
             for (int k = st; k < rows * 32; k += kSoftmaxThreads) {
-              const int row = n + (k >> 5), region = (k >> 3) & 3, c16 = k & 7;
-              *reinterpret_cast<uint4 *>(base + region * kRegionBytes + row * 128 + c16 * 16) =
+              const int row = n + (k >> 5), chunk = (k >> 3) & 3, c16 = k & 7;
+              *reinterpret_cast<uint4 *>(base + chunk * kChunkBytes + row * 128 + c16 * 16) =
                   make_uint4(0, 0, 0, 0);
             }
             fence_proxy_async_shared();
@@ -481,19 +565,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(smem_u32(&s.p_full));
+          // The last S of this segment has completed (its S was just read):
+          // Q of the next segment can go into tensor memory now, under the
+          // last P V and the epilogue.
+          if (last && have_next) load_q_own(nx.b);
         }
         if (!ok) break;
-        // ---- epilogue: O / l of this segment
-        if (!warp_wait(smem_u32(&s.pv_done), pv_ph, abort_flag)) {
+        // ---- epilogue: O / l of this segment, after its last P V
+        const uint32_t gl = g - 1;
+        if (!warp_wait(smem_u32(&s.pv_done[gl & 1u]), (gl >> 1) & 1u, abort_flag)) {
           if (lane == 0) set_abort(s, prm.dev_status);
           break;
         }
-        pv_ph ^= 1u;
         tc_fence_after();
         const float inv = 1.f / l;
         const float lse_val = (m_used + log2f(l)) * 0.69314718055994531f;
         if (!split) {
-          uint4 *dst = (uint4 *)(prm.out + ((int64_t)b * kHeads + h) * kVDim + rank * kVHalf);
+          uint4 *dst = (uint4 *)(prm.out + ((int64_t)b * kHeads + h) * kVDim + half * kVHalf);
 #pragma unroll 1
           for (int c = 0; c < kVHalf; c += 32) {
             uint32_t o[32];
@@ -507,10 +595,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                   pack_bf16(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv),
                   pack_bf16(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv));
           }
-          if (prm.lse && rank == 0) prm.lse[(int64_t)b * kHeads + h] = lse_val;
+          if (prm.lse && half == 0) prm.lse[(int64_t)b * kHeads + h] = lse_val;
         } else {
           const int slot = partial_slot(pair, it.U, it.P, Ub);
-          float4 *dst = (float4 *)(v.o_part + ((int64_t)slot * kHeads + h) * kVDim + rank * kVHalf);
+          float4 *dst = (float4 *)(v.o_part + ((int64_t)slot * kHeads + h) * kVDim + half * kVHalf);
 #pragma unroll 1
           for (int c = 0; c < kVHalf; c += 32) {
             uint32_t o[32];
@@ -522,14 +610,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                   __uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
                   __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
           }
-          if (rank == 0) v.lse_part[(int64_t)slot * kHeads + h] = lse_val;
+          if (half == 0) v.lse_part[(int64_t)slot * kHeads + h] = lse_val;
         }
         tc_fence_before();
-      }
-      if (!ok || s.abort) {
-        // on abort, wait (briefly) for any score the peer is still sending us
-        (void)mbar_wait<true>(smem_u32(&s.recv_full[xcount & 1]), (xcount >> 1) & 1u, nullptr,
-                              kDrainBudgetNs);
+        // advance to the next segment (already peeked)
+        it = nx;
+        t0 = nt0;
+        t1 = nt1;
+        split = nsplit;
+        Ub = nUb;
+        have = have_next;
       }
     }
   }
@@ -537,7 +627,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // ------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // no DSMEM traffic from the peer may outlive this CTA
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
@@ -570,24 +659,40 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-bool encode_cache_map(CUtensorMap *m, const void *cache, int64_t rows, uint32_t box_cols,
-                      uint32_t box_rows, CUtensorMapSwizzle sw) {
+// [rows x 576] bf16 (row stride 1152 B) read in boxes {64 columns, box_rows}.
+bool encode_2d(CUtensorMap *m, const void *base, int64_t rows, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)kRow, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)kRow * 2};
-  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(cache), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The same rows viewed as {64 columns, rows, 9 chunks of 64 columns}: a box
+// {64, box_rows, chunks} lands in shared memory chunk after chunk, each chunk
+// box_rows x 128 B.
+bool encode_3d(CUtensorMap *m, const void *base, int64_t rows, uint32_t box_rows,
+               uint32_t chunks) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(kRow / 64)};
+  cuuint64_t strides[2] = {(cuuint64_t)kRow * 2, 128};
+  cuuint32_t box[3] = {64, box_rows, chunks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 }  // namespace
 
 int tc_unit_tokens() { return tc::kTile; }
 
-// CTA pairs of the tensor-core kernel that can be resident at once on the
-// current device (clusters of 2 need both SMs in one GPC), capped at SMs / 2.
+// Split ranges of the tensor-core kernel: one per pair of SMs (two CTAs of
+// one SM each work on a range).
 int tc_max_pairs() {
   static int cached[64] = {0};
   int dev = 0;
@@ -595,35 +700,24 @@ int tc_max_pairs() {
   if (cached[dev] > 0) return cached[dev];
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-  const size_t smem = sizeof(tc::Smem) + 1024;
-  if (cudaFuncSetAttribute(tc::decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
-    return -1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
-  cfg.blockDim = dim3(tc::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, tc::decode_tc_kernel, &cfg) != cudaSuccess ||
-      clusters <= 0)
-    clusters = sms / 2;
-  cached[dev] = clusters < sms / 2 ? clusters : sms / 2;
+  cached[dev] = sms / 2 > 0 ? sms / 2 : 1;
   return cached[dev];
 }
-
-size_t tc_smem_bytes() { return sizeof(tc::Smem) + 1024; }
 
 cudaError_t launch_decode_tc(const void *q, const void *cache, int64_t num_blocks, int32_t block_size,
                              const int32_t *block_table, int32_t max_blocks_per_seq, int32_t batch,
                              float softmax_scale, void *out, float *lse, void *ws,
                              int32_t max_ranges, int32_t *dev_status, cudaStream_t stream) {
-  CUtensorMap map_v, map_r;
-  const uint32_t box_rows = block_size < tc::kTile ? (uint32_t)block_size : (uint32_t)tc::kTile;
+  tc::Maps maps;
   const int64_t rows = num_blocks * (int64_t)block_size;
-  if (!encode_cache_map(&map_v, cache, rows, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_cache_map(&map_r, cache, rows, 32, box_rows, CU_TENSOR_MAP_SWIZZLE_64B))
+  const uint32_t box_rows = block_size < tc::kTile ? (uint32_t)block_size : (uint32_t)tc::kTile;
+  const uint32_t rows3 = block_size < tc::kTile ? (uint32_t)block_size : (uint32_t)tc::kTile;
+  if (!encode_2d(&maps.kv2d, cache, rows, box_rows) ||
+      !encode_3d(&maps.kv5, cache, rows, rows3, 5) || !encode_3d(&maps.kv4, cache, rows, rows3, 4) ||
+      !encode_3d(&maps.kv1, cache, rows, rows3, 1) || !encode_3d(&maps.kv9, cache, rows, rows3, 9) ||
+      !encode_2d(&maps.q, q, (int64_t)batch * kHeads, kHeads))
     return cudaErrorInvalidValue;
-  const size_t smem = tc_smem_bytes();
+  const size_t smem = sizeof(tc::Smem) + 1024;
   cudaError_t e = cudaFuncSetAttribute(tc::decode_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -640,7 +734,7 @@ cudaError_t launch_decode_tc(const void *q, const void *cache, int64_t num_block
   p.ws = ws;
   p.max_ranges = max_ranges;
   p.dev_status = dev_status;
-  tc::decode_tc_kernel<<<2 * max_ranges, tc::kThreads, smem, stream>>>(map_v, map_r, p);
+  tc::decode_tc_kernel<<<2 * max_ranges, tc::kThreads, smem, stream>>>(maps, p);
   return cudaGetLastError();
 }
 
