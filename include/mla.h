@@ -140,9 +140,10 @@ mla_status_t mla_decode_plan(const int32_t *seq_lens, int32_t batch, int32_t num
  *   out           bf16 [batch, num_heads, 512] (written).
  *   lse           fp32 [batch, num_heads] natural-log sum-exp, or NULL.
  *   workspace     device scratch of >= mla_decode_workspace_size(batch,
- *                 num_heads) bytes, 256-byte aligned, zero-filled before its
- *                 first use.  Calls leave it ready for the next call; calls
- *                 sharing one workspace must not overlap on the GPU.
+ *                 num_heads) bytes, 256-byte aligned; its contents on entry
+ *                 do not matter (the plan rewrites everything the decode
+ *                 reads).  Calls sharing one workspace must not overlap on
+ *                 the GPU.
  * Requirements: num_heads == 128; block_size in {16, 32, 64, 128, 256};
  * max_seq_len <= max_blocks_per_seq * block_size; batch >= 0 (0 = no-op).
  * Rows the plan does not cover (tails past seq_len, unused blocks) are never

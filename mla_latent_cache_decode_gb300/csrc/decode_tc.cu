@@ -65,8 +65,14 @@ struct __align__(1024) Smem {
   uint8_t other[kSlots][5][kChunkBytes]; // other 256 kv_c dims (4 chunks) + rope: 40 KB / slot
   uint8_t own[kSlots][4][kChunkBytes];   // own 256 value dims: 32 KB / slot
   uint64_t other_full[kSlots], other_empty[kSlots], own_full[kSlots], own_empty[kSlots];
-  uint64_t s_full[2], pv_done[2];  // per S buffer: S ready / P V of that buffer's tile done
-  uint64_t p_full, q_full, q_tmem, q_free, fin_qk, fin_pv;
+  // per S buffer: S ready / P written over it / P V of that buffer's tile done.
+  // P has one barrier per buffer: the softmax warps run independently, and a
+  // warp may already write the next tile's P while another is still on this
+  // one; a single 128-arrival barrier would then count arrivals of two tiles
+  // in one phase.  No warp gets two tiles ahead (S of tile g+2 waits for the
+  // P V of tile g), so two barriers suffice.
+  uint64_t s_full[2], p_full[2], pv_done[2];
+  uint64_t q_full, q_tmem, q_free, fin_qk, fin_pv;
   uint32_t tmem_base;
   int abort;
 };
@@ -182,9 +188,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.s_full[i]), 1);
+      mbar_init(smem_u32(&s.p_full[i]), kSoftmaxThreads);
       mbar_init(smem_u32(&s.pv_done[i]), 1);
     }
-    mbar_init(smem_u32(&s.p_full), kSoftmaxThreads);
     mbar_init(smem_u32(&s.q_full), 1);
     mbar_init(smem_u32(&s.q_tmem), kSoftmaxThreads);
     mbar_init(smem_u32(&s.q_free), 1);
@@ -416,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int32_t tt = t0; tt < t1; tt += kTile, ++g) {
           const int n = min(kTile, t1 - tt);
           const int slot = g % kSlots;
-          if (!mbar_wait(smem_u32(&s.p_full), g & 1u, abort_flag, kWaitBudgetNs)) {
+          if (!mbar_wait(smem_u32(&s.p_full[g & 1u]), (g >> 1) & 1u, abort_flag, kWaitBudgetNs)) {
             set_abort(s, prm.dev_status);
             ok = false;
             break;
@@ -564,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(smem_u32(&s.p_full));
+          mbar_arrive(smem_u32(&s.p_full[g & 1u]));
           // The last S of this segment has completed (its S was just read):
           // Q of the next segment can go into tensor memory now, under the
           // last P V and the epilogue.

@@ -355,6 +355,36 @@ def test_config4_skewed_sampled(mla):
     assert_close(host_f64(out)[[1, 7]], ref, "config4 short requests")
 
 
+@pytest.mark.parametrize("q_kind", ["normal", "sharp"])
+def test_config4_every_short_request_repeated(mla, q_kind):
+    """Ranges holding several segments (split and unsplit, the last of a
+    range among them), run ten times: every short request against the oracle
+    once, then each repeat bit-identical to the first.  A race between the
+    pipeline's roles shows up as a repeat that differs, or as garbage in a
+    block of heads."""
+    w = mi.workload(4)
+    dl, host = _device_layer_and_host(w, 0, q_kind)
+    ws = mla.make_workspace(w.batch)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = _gpu_layer(mla, dl, ws, status, planned=False)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    reqs = list(range(1, w.batch))
+    ref, ref_lse = _oracle_sample(host, reqs)
+    assert_close(host_f64(out)[reqs], ref, f"config4 {q_kind} short requests")
+    assert_lse_close(lse.cpu().numpy()[reqs], ref_lse)
+    first = out.clone()
+    for rep in range(9):
+        out2 = torch.empty_like(out)
+        lse2 = torch.empty_like(lse)
+        mla.mla_decode(dl["q"], dl["cache"], dl["block_table"], dl["seq_lens"],
+                       dl["softmax_scale"], out2, lse2, workspace=ws, dev_status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert torch.equal(out2.view(torch.int16), first.view(torch.int16)), f"repeat {rep}"
+        assert torch.equal(lse2, lse), f"repeat {rep} lse"
+
+
 def test_config5_mixed_fragmented_sampled(mla):
     w = mi.workload(5)
     bt = mi.make_block_table(mi.rng_for(5, 0, 1), w.seq_lens, w.block_size, w.num_blocks())
