@@ -27,12 +27,6 @@ cudaError_t launch_decode_tc(const void *q, const void *cache, int64_t num_block
                              const int32_t *block_table, int32_t max_blocks_per_seq, int32_t batch,
                              float softmax_scale, void *out, float *lse, void *ws,
                              int32_t max_ranges, int32_t *dev_status, cudaStream_t stream);
-int simt_unit_tokens();
-cudaError_t launch_decode_simt(const void *q, const void *cache, int64_t num_blocks,
-                               int32_t block_size, const int32_t *block_table,
-                               int32_t max_blocks_per_seq, int32_t batch, float softmax_scale,
-                               void *out, float *lse, void *ws, int32_t max_ranges,
-                               int32_t *dev_status, cudaStream_t stream);
 
 namespace {
 
@@ -238,7 +232,7 @@ mla_status_t mla_combine(const float *o_partial, const float *lse_partial,
     return fail(MLA_ERR_INVALID_ARGUMENT, "null pointer");
   if (!aligned(o_partial, 16) || !aligned(out, 16) || !aligned(lse_partial, 4))
     return fail(MLA_ERR_INVALID_ARGUMENT, "o_partial/out must be 16-byte aligned");
-  if (batch > 65535 * 1024) return fail(MLA_ERR_INVALID_ARGUMENT, "batch too large");
+  if (num_heads > 65535) return fail(MLA_ERR_INVALID_ARGUMENT, "num_heads %d > 65535", num_heads);
   cudaError_t e = launch_offsets_combine(o_partial, lse_partial, split_offsets, batch, num_heads,
                                          out, lse, (cudaStream_t)stream);
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "combine launch");

@@ -51,7 +51,8 @@ struct PlanHeader {
 //   int32 range_first[P_max]  first request with units in range p
 //   int32 counters[B * 2]     split arrival counters (left at zero)
 //   fp32 lse_part[2 * P_max * H]
-//   fp32 o_part[2 * P_max * H * 512]
+//   fp32 o_part[2 * P_max][512 / 4][H][4]   (one partial's heads of four
+//                                            dims are contiguous)
 struct WorkspaceLayout {
   size_t seq_len, unit_prefix, range_first, counters, lse_part, o_part, total;
 };

@@ -18,9 +18,10 @@
 // more than recomputing them), then P V for its half.  Both CTAs read the same
 // tiles at about the same time, so the second read is served by L2.
 //
-// Operands.  Q's 256 "own" kv_c dims live in tensor memory (A operand); its
-// other 256 dims and its 64 rope dims live in shared memory (A operand from a
-// shared-memory descriptor).  S is double-buffered in tensor memory, so the S
+// Operands.  Q's 256 "own" kv_c dims live in tensor memory (A operand: staged
+// in shared memory by TMA at each segment start and copied over with
+// tcgen05.cp); its other 256 dims and its 64 rope dims live in shared memory
+// (A operand from a shared-memory descriptor).  S is double-buffered in tensor memory, so the S
 // MMAs of the next tile run while the softmax works on this one; P (bf16) is
 // written over the S buffer it came from and read from there by P V.  A 64-token cache tile arrives by TMA in two large boxes,
 // 128-byte swizzled: the "other" part (the other 256 kv_c dims + 64 rope dims)
@@ -28,15 +29,20 @@
 // other dims first, then rope, then the own dims, so the other part of a slot
 // is released early and refilled 1.5 tiles ahead, while the own part (also the
 // V operand of P V) is held until P V and is needed only at the end of the
-// next-but-one S: two slots per part hide the load latency.  Upcoming tiles
-// are prefetched into L2 so that refills are served by L2.
+// next-but-one S: two slots per part hide the load latency.  (L2 prefetch of
+// upcoming tiles, whole or only their other part, measured slower here: it
+// adds TMA instructions on the producer's critical path and, at launch, a
+// burst that delays every CTA's first tiles.)
 //
-// Warp roles: warp 0 loads the own parts (and prefetches into L2); warp 3
-// loads Q's other half per segment and the other parts; warp 1 issues the S
-// MMAs (and owns the tensor memory allocation); warp 2 issues the P V MMAs;
-// warps 4-7 (one thread per head) load Q into tensor memory, run the online
-// softmax with lazy rescaling of O, and write the output (or split partials
-// plus log-sum-exp).
+// Warp roles: warp 0 loads the own parts; warp 3
+// loads Q's other half per segment and the other parts; warps 1 and 8 issue
+// the S MMAs of even and odd tiles (warp 1 owns the tensor memory
+// allocation); warp 2 issues the P V MMAs;
+// warps 4-7 (one thread per head) run the online softmax with lazy rescaling
+// of O and write the output (or split partials plus log-sum-exp).
+#include <atomic>
+#include <mutex>
+
 #include "common.cuh"
 #include "sm100.cuh"
 
@@ -50,17 +56,21 @@ constexpr int kSlots = 2;                  // slots per part
 constexpr int kVHalf = 256;                // output dims per CTA
 constexpr int kChunkBytes = kTile * 128;   // one 64-dim, 64-token SW128 chunk: 8 KB
 constexpr int kQChunkBytes = 128 * 128;    // one 64-dim chunk of Q for 128 heads: 16 KB
-constexpr int kThreads = 256;              // 8 warps
+constexpr int kThreads = 288;              // 9 warps
 constexpr int kSoftmaxThreads = 128;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;  // S buffers at kColS + 64 * (g & 1)
 constexpr uint64_t kWaitBudgetNs = 100000000ull;  // 100 ms per wait, far above any legal wait
 constexpr uint64_t kDrainBudgetNs = 10000000ull;  // 10 ms to drain in-flight copies on abort
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
-constexpr int kPrefetchTiles = 4;                 // tiles prefetched into L2 ahead of the loads
+constexpr int kTabAhead = 4;                      // tiles the block-table entries are fetched ahead
+constexpr int kTabRing = 8;                       // ring of fetched entries (> kTabAhead)
+constexpr int kOtherAhead = 2;                    // other part prefetched into L2 this many tiles
+                                                  // ahead (0: off; < kTabAhead)
 
 struct __align__(1024) Smem {
   uint8_t q_other[4][kQChunkBytes];      // Q[:, other 256 dims], 4 chunks of 64 dims: 64 KB
+                                         // (at a segment start: Q[:, own dims], staged)
   uint8_t q_rope[kQChunkBytes];          // Q[:, 64 rope dims]: 16 KB
   uint8_t other[kSlots][5][kChunkBytes]; // other 256 kv_c dims (4 chunks) + rope: 40 KB / slot
   uint8_t own[kSlots][4][kChunkBytes];   // own 256 value dims: 32 KB / slot
@@ -72,7 +82,9 @@ struct __align__(1024) Smem {
   // in one phase.  No warp gets two tiles ahead (S of tile g+2 waits for the
   // P V of tile g), so two barriers suffice.
   uint64_t s_full[2], p_full[2], pv_done[2];
-  uint64_t q_full, q_tmem, q_free, fin_qk, fin_pv;
+  uint64_t qown_full, q_full, q_tmem, q_free, fin_qk, fin_pv;
+  // upcoming tiles, per producer: block-table entries [0, 4), first token [4]
+  int32_t tab[2][kTabRing][8];
   uint32_t tmem_base;
   int abort;
 };
@@ -82,7 +94,7 @@ struct __align__(1024) Smem {
 // chunks of 64 rows in one box, laid out chunk after chunk; the 2-D view
 // serves pages shorter than a tile.
 struct Maps {
-  CUtensorMap kv5, kv4, kv1, kv9, kv2d, q;
+  CUtensorMap kv5, kv4, kv1, kv2d, q;
 };
 
 struct Params {
@@ -146,29 +158,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// Rows of one tile: the cache row of each page-sized (or tile-sized) box.
-struct TileRows {
-  int boxes;
-  int32_t y[kTile / 16];
-};
-
-__device__ __forceinline__ TileRows tile_rows(const int32_t *table, int32_t tt, int n, int BS,
-                                              int box_rows, int64_t nb, int32_t *dev_status,
-                                              bool report_bad) {
-  TileRows r;
-  r.boxes = (n + box_rows - 1) / box_rows;
-  for (int j = 0; j < r.boxes; ++j) {
-    const int32_t tok = tt + j * box_rows;
-    int32_t blk = table[tok / BS];
-    if (blk < 0 || blk >= nb) {
-      if (report_bad) report(dev_status, MLA_ERR_DEVICE_RANGE);
-      blk = 0;
-    }
-    r.y[j] = blk * BS + (tok % BS);
-  }
-  return r;
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ Maps maps, const Params prm) {
   extern __shared__ uint8_t smem_raw[];
@@ -191,10 +180,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&s.p_full[i]), kSoftmaxThreads);
       mbar_init(smem_u32(&s.pv_done[i]), 1);
     }
+    mbar_init(smem_u32(&s.qown_full), 1);
     mbar_init(smem_u32(&s.q_full), 1);
-    mbar_init(smem_u32(&s.q_tmem), kSoftmaxThreads);
-    mbar_init(smem_u32(&s.q_free), 1);
-    mbar_init(smem_u32(&s.fin_qk), 1);
+    mbar_init(smem_u32(&s.q_tmem), 1);  // tcgen05.commit of the Q-own copy
+    mbar_init(smem_u32(&s.q_free), 2);  // both S issuers
+    mbar_init(smem_u32(&s.fin_qk), 2);
     mbar_init(smem_u32(&s.fin_pv), 1);
     s.abort = 0;
     fence_mbarrier_init_cluster();
@@ -219,7 +209,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producers
     if (active && elect_one_sync()) {
       const bool own_role = (warp == 0);
-      const uint64_t policy = policy_evict_first();
+      // normal priority: the pair's other CTA reads every tile too, usually a
+      // little later; evict-first lines were often gone by then (ncu: ~19%
+      // extra DRAM reads on a 64 x 4096 layer)
+      const uint64_t policy = policy_evict_normal();
       SegIter it;
       it.init(v, prm.batch, pair);
       int32_t t0, t1, Ub;
@@ -228,31 +221,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int box_rows = BS < kTile ? BS : kTile;
       const uint32_t box_bytes = (uint32_t)(box_rows * 128);
       const int64_t nb = prm.num_blocks;
-      // a second cursor walks the same tiles kPrefetchTiles ahead and asks L2
-      // for them (the own-part producer only)
-      SegIter pf;
-      pf.init(v, prm.batch, pair);
-      int32_t pf_t = 0, pf_t1 = 0, pf_Ub;
-      bool pf_split, pf_more = own_role;
-      auto prefetch_one = [&]() {
-        while (pf_more && pf_t >= pf_t1) pf_more = pf.next(pf_t, pf_t1, pf_split, pf_Ub);
-        if (!pf_more) return;
-        const int32_t *tab = prm.block_table + (int64_t)pf.b * prm.max_blocks_per_seq;
-        const TileRows r = tile_rows(tab, pf_t, min(kTile, pf_t1 - pf_t), BS, box_rows, nb,
-                                     prm.dev_status, false);
-        for (int j = 0; j < r.boxes; ++j) {
-          if (big_pages) {
-            tma_prefetch_3d(&maps.kv9, 0, r.y[j], 0);
-          } else {
-            for (int c = 0; c < 9; ++c) tma_prefetch_2d(&maps.kv2d, 64 * c, r.y[j]);
-          }
+      // Block-table entries of upcoming tiles are fetched kTabAhead tiles
+      // ahead by cp.async into a small ring: a plain load here would stall
+      // this thread for a memory latency on every tile before its copy could
+      // be issued.
+      int32_t *tab = &s.tab[own_role ? 0 : 1][0][0];
+      SegIter fc;
+      fc.init(v, prm.batch, pair);
+      int32_t fc_t = 0, fc_t1 = 0, fc_Ub;
+      bool fc_split, fc_more = true;
+      uint32_t fc_g = 0;
+      auto fetch_next = [&]() {  // entries of the next tile (if any), as one group
+        while (fc_more && fc_t >= fc_t1) fc_more = fc.next(fc_t, fc_t1, fc_split, fc_Ub);
+        if (fc_more) {
+          const int32_t *row = prm.block_table + (int64_t)fc.b * prm.max_blocks_per_seq;
+          const int nbx = (min(kTile, fc_t1 - fc_t) + box_rows - 1) / box_rows;
+          int32_t *dst = tab + (fc_g % kTabRing) * 8;
+          for (int j = 0; j < nbx; ++j) cp_async_4(smem_u32(dst + j), row + (fc_t + j * box_rows) / BS);
+          dst[4] = fc_t;
+          fc_t += kTile;
+          ++fc_g;
         }
-        pf_t += kTile;
+        cp_async_commit();
       };
+      for (int i = 0; i < kTabAhead; ++i) fetch_next();
       if (own_role) {
         prefetch_tmap(&maps.kv4);
-        prefetch_tmap(&maps.kv9);
-        for (int i = 0; i < kPrefetchTiles; ++i) prefetch_one();
       } else {
         prefetch_tmap(&maps.kv5);
         prefetch_tmap(&maps.kv1);
@@ -261,23 +255,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       while (ok && it.next(t0, t1, split, Ub)) {
         if (!own_role) {
-          // Q[:, other 256 dims] of request b into shared memory
+          // Q of request b, once the previous segment's S MMAs are done with
+          // it: first its own 256 dims (and rope) into the Q buffers, from
+          // where the even S issuer copies the own dims into tensor memory
+          // (tcgen05.cp), then, once copied, its other 256 dims.
           if (!mbar_wait(smem_u32(&s.q_free), (seg & 1u) ^ 1u, abort_flag, kWaitBudgetNs)) {
             set_abort(s, prm.dev_status);
             break;
           }
-          mbar_arrive_expect_tx(smem_u32(&s.q_full), 5 * kQChunkBytes);
+          mbar_arrive_expect_tx(smem_u32(&s.qown_full), 5 * kQChunkBytes);
+          for (int c = 0; c < 4; ++c)
+            tma_load_2d(smem_u32(s.q_other[c]), &maps.q, 64 * (own0 + c), it.b * kHeads,
+                        smem_u32(&s.qown_full));
+          tma_load_2d(smem_u32(s.q_rope), &maps.q, 512, it.b * kHeads, smem_u32(&s.qown_full));
+          {  // the next segment's Q rows into L2 meanwhile
+            SegIter nx = it;
+            int32_t a0, a1, aU;
+            bool asplit;
+            if (nx.next(a0, a1, asplit, aU))
+              for (int c = 0; c < 9; ++c) tma_prefetch_2d(&maps.q, 64 * c, nx.b * kHeads);
+          }
+          if (!mbar_wait(smem_u32(&s.q_tmem), seg & 1u, abort_flag, kWaitBudgetNs)) {
+            set_abort(s, prm.dev_status);
+            break;
+          }
+          mbar_arrive_expect_tx(smem_u32(&s.q_full), 4 * kQChunkBytes);
           for (int c = 0; c < 4; ++c)
             tma_load_2d(smem_u32(s.q_other[c]), &maps.q, 64 * (oth0 + c), it.b * kHeads,
                         smem_u32(&s.q_full));
-          tma_load_2d(smem_u32(s.q_rope), &maps.q, 512, it.b * kHeads, smem_u32(&s.q_full));
         }
         ++seg;
-        const int32_t *table = prm.block_table + (int64_t)it.b * prm.max_blocks_per_seq;
         for (int32_t tt = t0; tt < t1; tt += kTile, ++g) {
-          if (own_role) prefetch_one();
-          const TileRows r = tile_rows(table, tt, min(kTile, t1 - tt), BS, box_rows, nb,
-                                       prm.dev_status, own_role);
+          fetch_next();
+          // this tile's entries (and those of the tile kOtherAhead later) have landed
+          cp_async_wait<kTabAhead - kOtherAhead>();
+          // cache rows of the tile's boxes (one box per page, or one per tile)
+          const int nbx = (min(kTile, t1 - tt) + box_rows - 1) / box_rows;
+          const int32_t *e = tab + (g % kTabRing) * 8;
+          int32_t y[kTile / 16];
+#pragma unroll
+          for (int j = 0; j < kTile / 16; ++j) {
+            if (j >= nbx) break;
+            int32_t blk = e[j];
+            if (blk < 0 || blk >= nb) {
+              if (own_role) report(prm.dev_status, MLA_ERR_DEVICE_RANGE);
+              blk = 0;
+            }
+            y[j] = blk * BS + ((tt + j * box_rows) % BS);
+          }
           const int slot = g % kSlots;
           const uint32_t par = ((g / kSlots) & 1u) ^ 1u;
           if (own_role) {
@@ -287,14 +312,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             const uint32_t bar = smem_u32(&s.own_full[slot]);
-            mbar_arrive_expect_tx(bar, 4u * r.boxes * box_bytes);
+            mbar_arrive_expect_tx(bar, 4u * nbx * box_bytes);
             if (big_pages) {
-              tma_load_3d_hint(smem_u32(s.own[slot][0]), &maps.kv4, 0, r.y[0], own0, bar, policy);
+              tma_load_3d_hint(smem_u32(s.own[slot][0]), &maps.kv4, 0, y[0], own0, bar, policy);
             } else {
-              for (int j = 0; j < r.boxes; ++j)
+#pragma unroll
+              for (int j = 0; j < kTile / 16; ++j) {
+                if (j >= nbx) break;
                 for (int c = 0; c < 4; ++c)
                   tma_load_2d_hint(smem_u32(s.own[slot][c]) + j * box_bytes, &maps.kv2d,
-                                   64 * (own0 + c), r.y[j], bar, policy);
+                                   64 * (own0 + c), y[j], bar, policy);
+              }
             }
           } else {
             if (!mbar_wait(smem_u32(&s.other_empty[slot]), par, abort_flag, kWaitBudgetNs)) {
@@ -303,33 +331,63 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             const uint32_t bar = smem_u32(&s.other_full[slot]);
-            mbar_arrive_expect_tx(bar, 5u * r.boxes * box_bytes);
+            mbar_arrive_expect_tx(bar, 5u * nbx * box_bytes);
             if (big_pages) {
               if (half == 0) {  // other = chunks 4..7, rope = chunk 8: contiguous
-                tma_load_3d_hint(smem_u32(s.other[slot][0]), &maps.kv5, 0, r.y[0], 4, bar, policy);
+                tma_load_3d_hint(smem_u32(s.other[slot][0]), &maps.kv5, 0, y[0], 4, bar, policy);
               } else {          // other = chunks 0..3, then rope
-                tma_load_3d_hint(smem_u32(s.other[slot][0]), &maps.kv4, 0, r.y[0], 0, bar, policy);
-                tma_load_3d_hint(smem_u32(s.other[slot][4]), &maps.kv1, 0, r.y[0], 8, bar, policy);
+                tma_load_3d_hint(smem_u32(s.other[slot][0]), &maps.kv4, 0, y[0], 0, bar, policy);
+                tma_load_3d_hint(smem_u32(s.other[slot][4]), &maps.kv1, 0, y[0], 8, bar, policy);
               }
             } else {
-              for (int j = 0; j < r.boxes; ++j)
+#pragma unroll
+              for (int j = 0; j < kTile / 16; ++j) {
+                if (j >= nbx) break;
                 for (int c = 0; c < 5; ++c)
                   tma_load_2d_hint(smem_u32(s.other[slot][c]) + j * box_bytes, &maps.kv2d,
-                                   c < 4 ? 64 * (oth0 + c) : 512, r.y[j], bar, policy);
+                                   c < 4 ? 64 * (oth0 + c) : 512, y[j], bar, policy);
+              }
+            }
+            if (kOtherAhead > 0 && big_pages && g + kOtherAhead < fc_g) {
+              // L2 prefetch of the other part of the tile kOtherAhead later
+              // (its entries are in the ring; a slot is refilled only when it
+              // frees, too late to hide an HBM read)
+              const int32_t *e2 = tab + ((g + kOtherAhead) % kTabRing) * 8;
+              int32_t blk = e2[0];
+              if (blk >= 0 && blk < nb) {
+                const int32_t y2 = blk * BS + (e2[4] % BS);
+                if (half == 0) {
+                  tma_prefetch_3d(&maps.kv5, 0, y2, 4);
+                } else {
+                  tma_prefetch_3d(&maps.kv4, 0, y2, 0);
+                  tma_prefetch_3d(&maps.kv1, 0, y2, 8);
+                }
+              }
             }
           }
         }
       }
+      cp_async_wait<0>();  // no copy into the ring outlives the thread
       if (s.abort) {
         // the consumers gave up: let the last issued loads land before exit
         for (int i = 0; i < kSlots; ++i)
           (void)mbar_wait(smem_u32(own_role ? &s.own_full[i] : &s.other_full[i]), 0, nullptr,
                           kDrainBudgetNs);
-        if (!own_role) (void)mbar_wait(smem_u32(&s.q_full), 0, nullptr, kDrainBudgetNs);
+        if (!own_role) {
+          (void)mbar_wait(smem_u32(&s.qown_full), 0, nullptr, kDrainBudgetNs);
+          (void)mbar_wait(smem_u32(&s.q_full), 0, nullptr, kDrainBudgetNs);
+        }
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ S = Q K^T issuer
+  } else if (warp == 1 || warp == 8) {
+    // ------------------------------------------------------------ S = Q K^T issuers
+    // Warp 1 issues the S MMAs of even tiles, warp 8 those of odd tiles: one
+    // thread cannot issue N = 64 MMAs as fast as the tensor pipe runs them.
+    // Tile g uses S buffer g & 1 and ring slot g % 2, so the two never touch
+    // the same accumulator or operands.  Both wait for every segment's Q and
+    // both release it (q_free counts two arrivals); the even issuer also
+    // copies the segment's Q own dims into tensor memory.
+    const uint32_t par = warp == 8 ? 1u : 0u;
     if (active && elect_one_sync()) {
       SegIter it;
       it.init(v, prm.batch, pair);
@@ -347,19 +405,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t a_q = tmem + kColQ;
       bool ok = true;
       while (ok && it.next(t0, t1, split, Ub)) {
-        if (!mbar_wait(smem_u32(&s.q_full), seg & 1u, abort_flag, kWaitBudgetNs) ||
-            !mbar_wait(smem_u32(&s.q_tmem), seg & 1u, abort_flag, kWaitBudgetNs)) {
+        if (!mbar_wait(smem_u32(&s.qown_full), seg & 1u, abort_flag, kWaitBudgetNs)) {
+          set_abort(s, prm.dev_status);
+          break;
+        }
+        if (par == 0) {
+          // Q[:, own 256 dims] (staged in the Q buffers) into tensor memory:
+          // 16 copies of 128 rows x 16 dims, addressed like the A operand
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tmem_cp_128x256b(a_q + c * 32 + kk * 8,
+                               d_q + (uint64_t)((c * kQChunkBytes + kk * 32) >> 4));
+          mma_commit(smem_u32(&s.q_tmem));
+        }
+        if (!mbar_wait(smem_u32(&s.q_tmem), seg & 1u, abort_flag, kWaitBudgetNs) ||
+            !mbar_wait(smem_u32(&s.q_full), seg & 1u, abort_flag, kWaitBudgetNs)) {
           set_abort(s, prm.dev_status);
           break;
         }
         ++seg;
         tc_fence_after();
         for (int32_t tt = t0; tt < t1; tt += kTile, ++g) {
+          if ((g & 1u) != par) continue;  // the other issuer's tile
           const int slot = g % kSlots;
-          const uint32_t par = (g / kSlots) & 1u;
+          const uint32_t ph = (g / kSlots) & 1u;
           const uint32_t d_s = tmem + kColS + 64 * (g & 1u);
           // the S buffer is free once P V of tile g-2 (which read P from it) is done
-          if (!mbar_wait(smem_u32(&s.other_full[slot]), par, abort_flag, kWaitBudgetNs) ||
+          if (!mbar_wait(smem_u32(&s.other_full[slot]), ph, abort_flag, kWaitBudgetNs) ||
               (g >= 2 && !mbar_wait(smem_u32(&s.pv_done[g & 1u]), ((g >> 1) - 1) & 1u, abort_flag,
                                     kWaitBudgetNs))) {
             set_abort(s, prm.dev_status);
@@ -384,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        bo + (uint64_t)((4 * kChunkBytes + kk * 32) >> 4), id);
           mma_commit(smem_u32(&s.other_empty[slot]));
           // own 256 kv_c dims: A = Q (tensor memory), B = own part
-          if (!mbar_wait(smem_u32(&s.own_full[slot]), par, abort_flag, kWaitBudgetNs)) {
+          if (!mbar_wait(smem_u32(&s.own_full[slot]), ph, abort_flag, kWaitBudgetNs)) {
             set_abort(s, prm.dev_status);
             ok = false;
             break;
@@ -442,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(smem_u32(&s.fin_pv), 0, nullptr, kWaitBudgetNs))
         report(prm.dev_status, MLA_ERR_DEVICE_TIMEOUT);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ softmax / epilogue
     const int q4 = warp & 3;              // TMEM lane quadrant of this warp
     const int h = q4 * 32 + lane;         // head = TMEM lane
@@ -459,19 +534,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (active) {
-      // Q[h, own 256 dims] of request qb into tensor memory (A operand of S)
-      auto load_q_own = [&](int qb) {
-        const uint4 *qrow = (const uint4 *)(prm.q + ((int64_t)qb * kHeads + h) * kRow);
-        uint4 buf[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) buf[k] = __ldg(qrow + half * 32 + k);
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          tmem_st16(lane_addr + kColQ + 16 * c, reinterpret_cast<const uint32_t *>(&buf[4 * c]));
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(smem_u32(&s.q_tmem));
-      };
       SegIter it;
       it.init(v, prm.batch, pair);
       int32_t t0, t1, Ub;
@@ -479,7 +541,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t g = 0;  // tiles so far
       bool ok = true;
       bool have = it.next(t0, t1, split, Ub);
-      if (have) load_q_own(it.b);
       while (ok && have) {
         const int b = it.b;
         SegIter nx = it;  // the segment after this one, if any
@@ -490,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_used = -INFINITY, l = 0.f;
         for (int32_t tt = t0; tt < t1; tt += kTile, ++g) {
           const int n = min(kTile, t1 - tt);
-          const bool first = (tt == t0), last = (tt + kTile >= t1);
+          const bool first = (tt == t0);
           const uint32_t buf_col = kColS + 64 * (g & 1u);
           if (!warp_wait(smem_u32(&s.s_full[g & 1u]), (g >> 1) & 1u, abort_flag)) {
             if (lane == 0) set_abort(s, prm.dev_status);
@@ -571,10 +632,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(smem_u32(&s.p_full[g & 1u]));
-          // The last S of this segment has completed (its S was just read):
-          // Q of the next segment can go into tensor memory now, under the
-          // last P V and the epilogue.
-          if (last && have_next) load_q_own(nx.b);
         }
         if (!ok) break;
         // ---- epilogue: O / l of this segment, after its last P V
@@ -603,8 +660,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (prm.lse && half == 0) prm.lse[(int64_t)b * kHeads + h] = lse_val;
         } else {
+          // partials are stored as [slot][dim / 4][head][4]: a warp's 32 heads
+          // of four dims are 512 contiguous bytes, so every float4 store
+          // coalesces (head-major rows, one per thread, cost a line per lane)
           const int slot = partial_slot(pair, it.U, it.P, Ub);
-          float4 *dst = (float4 *)(v.o_part + ((int64_t)slot * kHeads + h) * kVDim + half * kVHalf);
+          float4 *dst = reinterpret_cast<float4 *>(v.o_part) +
+                        ((int64_t)slot * (kVDim / 4) + half * (kVHalf / 4)) * kHeads + h;
 #pragma unroll 1
           for (int c = 0; c < kVHalf; c += 32) {
             uint32_t o[32];
@@ -612,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_ld();
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-              dst[c / 4 + k] = make_float4(
+              dst[(int64_t)(c / 4 + k) * kHeads] = make_float4(
                   __uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
                   __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
           }
@@ -710,22 +771,97 @@ int tc_max_pairs() {
   return cached[dev];
 }
 
+namespace {
+// Tensor maps depend only on the tensor's address and shape, so they are
+// encoded once and kept in small direct-mapped caches (a decode step touches
+// one cache and one q tensor per layer: 61 of each for a DeepSeek-V3 step).
+// Eager callers then pay no encode per call; graph replays never did.
+struct KvEntry {
+  bool valid;
+  int dev;
+  const void *base;
+  int64_t rows;
+  int32_t block_size;
+  CUtensorMap kv5, kv4, kv1, kv2d;
+};
+struct QEntry {
+  bool valid;
+  int dev;
+  const void *base;
+  int32_t batch;
+  CUtensorMap q;
+};
+constexpr int kMapCacheSize = 256;
+std::mutex g_map_mu;
+KvEntry g_kv_maps[kMapCacheSize];
+QEntry g_q_maps[kMapCacheSize];
+
+size_t slot_of_ptr(const void *p) {
+  const uint64_t x = (uint64_t)(uintptr_t)p;
+  return (size_t)((x >> 8) ^ (x >> 20) ^ (x >> 32)) % kMapCacheSize;
+}
+
+bool kv_maps(int dev, const void *cache, int64_t rows, int32_t block_size, tc::Maps *m) {
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  KvEntry &e = g_kv_maps[slot_of_ptr(cache)];
+  if (!(e.valid && e.dev == dev && e.base == cache && e.rows == rows && e.block_size == block_size)) {
+    const uint32_t box_rows = block_size < tc::kTile ? (uint32_t)block_size : (uint32_t)tc::kTile;
+    e.valid = false;
+    if (!encode_2d(&e.kv2d, cache, rows, box_rows) || !encode_3d(&e.kv5, cache, rows, box_rows, 5) ||
+        !encode_3d(&e.kv4, cache, rows, box_rows, 4) || !encode_3d(&e.kv1, cache, rows, box_rows, 1))
+      return false;
+    e.valid = true;
+    e.dev = dev;
+    e.base = cache;
+    e.rows = rows;
+    e.block_size = block_size;
+  }
+  m->kv5 = e.kv5;
+  m->kv4 = e.kv4;
+  m->kv1 = e.kv1;
+  m->kv2d = e.kv2d;
+  return true;
+}
+
+bool q_map(int dev, const void *q, int32_t batch, tc::Maps *m) {
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  QEntry &e = g_q_maps[slot_of_ptr(q)];
+  if (!(e.valid && e.dev == dev && e.base == q && e.batch == batch)) {
+    e.valid = false;
+    if (!encode_2d(&e.q, q, (int64_t)batch * kHeads, kHeads)) return false;
+    e.valid = true;
+    e.dev = dev;
+    e.base = q;
+    e.batch = batch;
+  }
+  m->q = e.q;
+  return true;
+}
+
+// the kernel's dynamic shared memory opt-in, set once per device
+cudaError_t ensure_smem_attr(int dev, size_t smem) {
+  static std::atomic<bool> done[64];
+  if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(tc::decode_tc_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
+  return e;
+}
+}  // namespace
+
 cudaError_t launch_decode_tc(const void *q, const void *cache, int64_t num_blocks, int32_t block_size,
                              const int32_t *block_table, int32_t max_blocks_per_seq, int32_t batch,
                              float softmax_scale, void *out, float *lse, void *ws,
                              int32_t max_ranges, int32_t *dev_status, cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
   tc::Maps maps;
-  const int64_t rows = num_blocks * (int64_t)block_size;
-  const uint32_t box_rows = block_size < tc::kTile ? (uint32_t)block_size : (uint32_t)tc::kTile;
-  const uint32_t rows3 = block_size < tc::kTile ? (uint32_t)block_size : (uint32_t)tc::kTile;
-  if (!encode_2d(&maps.kv2d, cache, rows, box_rows) ||
-      !encode_3d(&maps.kv5, cache, rows, rows3, 5) || !encode_3d(&maps.kv4, cache, rows, rows3, 4) ||
-      !encode_3d(&maps.kv1, cache, rows, rows3, 1) || !encode_3d(&maps.kv9, cache, rows, rows3, 9) ||
-      !encode_2d(&maps.q, q, (int64_t)batch * kHeads, kHeads))
+  if (!kv_maps(dev, cache, num_blocks * (int64_t)block_size, block_size, &maps) ||
+      !q_map(dev, q, batch, &maps))
     return cudaErrorInvalidValue;
   const size_t smem = sizeof(tc::Smem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(tc::decode_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  e = ensure_smem_attr(dev, smem);
   if (e != cudaSuccess) return e;
   tc::Params p;
   p.q = (const __nv_bfloat16 *)q;

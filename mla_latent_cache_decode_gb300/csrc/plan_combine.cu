@@ -103,101 +103,192 @@ cudaError_t launch_plan(const int32_t *seq_lens, int32_t batch, int32_t unit_tok
 }
 
 // ---------------------------------------------------------------------------
-// Combine: one warp per (request, head); lane k owns output dims 4k..4k+3 of
-// every 128-dim quarter.
+// Combine: one block of 128 threads per (request, head) row; thread t owns
+// output dims 4t..4t+3.  The partials were just written by the decode and sit
+// in L2, so the kernel is latency-bound: many rows in flight and the split
+// loop unrolled so that several partial loads are outstanding per thread.
 // ---------------------------------------------------------------------------
+constexpr int kCombineThreads = kVDim / 4;  // 128
+
 template <typename SlotFn>
-__device__ __forceinline__ void combine_head(const float *__restrict__ o_part,
-                                             const float *__restrict__ lse_part, int nsplit,
-                                             SlotFn slot, int h, int heads,
-                                             __nv_bfloat16 *__restrict__ out_row,
-                                             float *lse_out) {
-  const int lane = threadIdx.x & 31;
+__device__ __forceinline__ void combine_row(const float *__restrict__ o_part,
+                                            const float *__restrict__ lse_part, int nsplit,
+                                            SlotFn slot, int h, int heads,
+                                            __nv_bfloat16 *__restrict__ out_row,
+                                            float *lse_out) {
+  // The block's splits are taken kCombineThreads at a time: thread t works
+  // out the slot and log-sum-exp of split base + t once, in shared memory,
+  // and every thread of the block reads them from there.
+  __shared__ int64_t s_slot[kCombineThreads];
+  __shared__ float s_lse[kCombineThreads];
+  const int t = threadIdx.x;
   float m = -INFINITY;
-  for (int s = lane; s < nsplit; s += 32) m = fmaxf(m, lse_part[(int64_t)slot(s) * heads + h]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  float4 acc[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int base = 0; base < nsplit; base += kCombineThreads) {
+    const int cnt = min(kCombineThreads, nsplit - base);
+    __syncthreads();
+    if (t < cnt) {
+      const int64_t w = slot(base + t);
+      s_slot[t] = w;
+      s_lse[t] = lse_part[w * heads + h];
+    }
+    __syncthreads();
+    for (int k = 0; k < cnt; ++k) m = fmaxf(m, s_lse[k]);
+  }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float z = 0.f;
   if (m != -INFINITY) {
-    for (int s = 0; s < nsplit; ++s) {
-      const int64_t w = slot(s);
-      const float l = lse_part[w * heads + h];
-      if (l == -INFINITY) continue;
-      const float a = __expf(l - m);
-      z += a;
-      const float4 *src = (const float4 *)(o_part + (w * heads + h) * kVDim);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float4 x = src[lane + 32 * k];
-        acc[k].x += a * x.x; acc[k].y += a * x.y; acc[k].z += a * x.z; acc[k].w += a * x.w;
+    for (int base = 0; base < nsplit; base += kCombineThreads) {
+      const int cnt = min(kCombineThreads, nsplit - base);
+      if (nsplit > kCombineThreads) {  // else the table from the max pass is still in place
+        __syncthreads();
+        if (t < cnt) {
+          const int64_t w = slot(base + t);
+          s_slot[t] = w;
+          s_lse[t] = lse_part[w * heads + h];
+        }
+        __syncthreads();
+      }
+#pragma unroll 4
+      for (int k = 0; k < cnt; ++k) {
+        const float l = s_lse[k];
+        const float a = l == -INFINITY ? 0.f : __expf(l - m);
+        const float4 x =
+            __ldg(reinterpret_cast<const float4 *>(o_part + (s_slot[k] * heads + h) * kVDim) + t);
+        z += a;
+        acc.x += a * x.x; acc.y += a * x.y; acc.z += a * x.z; acc.w += a * x.w;
       }
     }
   }
   const float inv = z > 0.f ? 1.f / z : 0.f;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc[k].x * inv, acc[k].y * inv);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc[k].z * inv, acc[k].w * inv);
-    uint2 pk;
-    pk.x = *reinterpret_cast<uint32_t *>(&lo);
-    pk.y = *reinterpret_cast<uint32_t *>(&hi);
-    *reinterpret_cast<uint2 *>(out_row + 4 * (lane + 32 * k)) = pk;
-  }
-  if (lse_out && lane == 0) *lse_out = z > 0.f ? m + logf(z) : -INFINITY;
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  uint2 pk;
+  pk.x = *reinterpret_cast<uint32_t *>(&lo);
+  pk.y = *reinterpret_cast<uint32_t *>(&hi);
+  *reinterpret_cast<uint2 *>(out_row + 4 * t) = pk;
+  if (lse_out && t == 0) *lse_out = z > 0.f ? m + logf(z) : -INFINITY;
 }
 
-// Merges the partials of every split request of a plan.
-__global__ void __launch_bounds__(128) plan_combine_kernel(void *ws, int32_t batch, int32_t heads,
-                                                           int32_t max_ranges,
-                                                           __nv_bfloat16 *__restrict__ out,
-                                                           float *__restrict__ lse) {
-  PlanView v = plan_view(ws, batch, heads, max_ranges);
-  const int b = blockIdx.x;
-  const int h = blockIdx.y * 4 + (threadIdx.x >> 5);
-  if (h >= heads) return;
+// Merges the partials of every split request of a plan.  The decode stores
+// them as [slot][512 / 4][128][4], so in the block of (request, 16-dim block)
+// thread h = head reads four dims of its head per load (a warp's loads are
+// 512 contiguous bytes) and accumulates its 16 dims in registers; splits are
+// taken four at a time with all their loads issued before any is used, since
+// the kernel is latency-bound.  The bf16 results are transposed through
+// shared memory into the [B][H][512] output (32 bytes of a row per head).
+// grid = (batch, 512 / 16), 128 threads.
+constexpr int kCombDims = 16;
+constexpr int kCombGroup = 4;  // splits whose loads are in flight together
+
+__global__ void __launch_bounds__(kHeads) plan_combine_kernel(void *ws, int32_t batch,
+                                                              int32_t max_ranges,
+                                                              __nv_bfloat16 *__restrict__ out,
+                                                              float *__restrict__ lse) {
+  PlanView v = plan_view(ws, batch, kHeads, max_ranges);
+  const int b = blockIdx.x, d0 = blockIdx.y * kCombDims, h = threadIdx.x;
   const int32_t U = v.hdr->total_units, P = v.hdr->num_ranges;
   const int32_t Ub = v.unit_prefix[b], n = v.unit_prefix[b + 1] - Ub;
   if (n == 0) return;
   const int32_t p0 = range_of(Ub, U, P), p1 = range_of(Ub + n - 1, U, P);
   if (p0 == p1) return;
-  auto slot = [&](int s) { return partial_slot(p0 + s, U, P, Ub); };
-  combine_head(v.o_part, v.lse_part, p1 - p0 + 1, slot, h, heads,
-               out + ((int64_t)b * heads + h) * kVDim, lse ? lse + (int64_t)b * heads + h : nullptr);
+  const int nsplit = p1 - p0 + 1;
+  __shared__ int32_t s_slot[kHeads];
+  __shared__ __align__(16) __nv_bfloat16 tile[kHeads][kCombDims + 8];  // +8: stagger the rows
+  float4 acc[kCombDims / 4];
+#pragma unroll
+  for (int j = 0; j < kCombDims / 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float m = -INFINITY, z = 0.f;
+  // splits kHeads at a time (a request spans at most P <= max_ranges ranges);
+  // the running max rescales what was summed so far when a later chunk raises it
+  for (int base = 0; base < nsplit; base += kHeads) {
+    const int cnt = min(kHeads, nsplit - base);
+    __syncthreads();
+    if (h < cnt) s_slot[h] = partial_slot(p0 + base + h, U, P, Ub);
+    __syncthreads();
+    float mc = m;
+    for (int k = 0; k < cnt; ++k) mc = fmaxf(mc, v.lse_part[(int64_t)s_slot[k] * kHeads + h]);
+    if (mc == -INFINITY) continue;
+    if (m != -INFINITY && mc != m) {
+      const float r = __expf(m - mc);
+      z *= r;
+#pragma unroll
+      for (int j = 0; j < kCombDims / 4; ++j) {
+        acc[j].x *= r; acc[j].y *= r; acc[j].z *= r; acc[j].w *= r;
+      }
+    }
+    m = mc;
+    for (int k0 = 0; k0 < cnt; k0 += kCombGroup) {
+      float a[kCombGroup];
+      float4 x[kCombGroup][kCombDims / 4];
+#pragma unroll
+      for (int u = 0; u < kCombGroup; ++u) {
+        const bool live = k0 + u < cnt;
+        const int64_t w = s_slot[live ? k0 + u : k0];
+        const float l = v.lse_part[w * kHeads + h];
+        a[u] = (!live || l == -INFINITY) ? 0.f : __expf(l - m);
+        const float4 *src = reinterpret_cast<const float4 *>(v.o_part) +
+                            (w * (kVDim / 4) + d0 / 4) * kHeads + h;
+#pragma unroll
+        for (int j = 0; j < kCombDims / 4; ++j) x[u][j] = __ldg(src + (int64_t)j * kHeads);
+      }
+#pragma unroll
+      for (int u = 0; u < kCombGroup; ++u) {
+        z += a[u];
+#pragma unroll
+        for (int j = 0; j < kCombDims / 4; ++j) {
+          acc[j].x += a[u] * x[u][j].x; acc[j].y += a[u] * x[u][j].y;
+          acc[j].z += a[u] * x[u][j].z; acc[j].w += a[u] * x[u][j].w;
+        }
+      }
+    }
+  }
+  const float inv = z > 0.f ? 1.f / z : 0.f;
+#pragma unroll
+  for (int j = 0; j < kCombDims / 4; ++j) {
+    *reinterpret_cast<__nv_bfloat162 *>(&tile[h][4 * j]) =
+        __floats2bfloat162_rn(acc[j].x * inv, acc[j].y * inv);
+    *reinterpret_cast<__nv_bfloat162 *>(&tile[h][4 * j + 2]) =
+        __floats2bfloat162_rn(acc[j].z * inv, acc[j].w * inv);
+  }
+  __syncthreads();
+  // 128 rows x 32 bytes: two 16-byte pieces per row, thread t takes pieces t + 128 k
+  __nv_bfloat16 *orow = out + (int64_t)b * kHeads * kVDim + d0;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int piece = h + kHeads * k, row = piece >> 1, part = piece & 1;
+    *reinterpret_cast<uint4 *>(orow + (int64_t)row * kVDim + part * 8) =
+        *reinterpret_cast<const uint4 *>(&tile[row][part * 8]);
+  }
+  if (lse && blockIdx.y == 0) lse[(int64_t)b * kHeads + h] = z > 0.f ? m + logf(z) : -INFINITY;
 }
 
 cudaError_t launch_plan_combine(void *ws, int32_t batch, int32_t heads, int32_t max_ranges,
                                 void *out, float *lse, cudaStream_t stream) {
-  dim3 grid(batch, (heads + 3) / 4);
-  plan_combine_kernel<<<grid, 128, 0, stream>>>(ws, batch, heads, max_ranges,
-                                                (__nv_bfloat16 *)out, lse);
+  if (heads != kHeads) return cudaErrorInvalidValue;
+  dim3 grid(batch, kVDim / kCombDims);
+  plan_combine_kernel<<<grid, kHeads, 0, stream>>>(ws, batch, max_ranges,
+                                                   (__nv_bfloat16 *)out, lse);
   return cudaGetLastError();
 }
 
-// The public combine over caller-given split offsets.
-__global__ void __launch_bounds__(128) offsets_combine_kernel(const float *__restrict__ o_part,
-                                                              const float *__restrict__ lse_part,
-                                                              const int32_t *__restrict__ offsets,
-                                                              int32_t heads,
-                                                              __nv_bfloat16 *__restrict__ out,
-                                                              float *__restrict__ lse) {
-  const int b = blockIdx.x;
-  const int h = blockIdx.y * 4 + (threadIdx.x >> 5);
-  if (h >= heads) return;
+// The public combine over caller-given split offsets.  grid = (batch, heads).
+__global__ void __launch_bounds__(kCombineThreads) offsets_combine_kernel(
+    const float *__restrict__ o_part, const float *__restrict__ lse_part,
+    const int32_t *__restrict__ offsets, int32_t heads, __nv_bfloat16 *__restrict__ out,
+    float *__restrict__ lse) {
+  const int b = blockIdx.x, h = blockIdx.y;
   const int32_t w0 = offsets[b], w1 = offsets[b + 1];
   auto slot = [&](int s) { return w0 + s; };
-  combine_head(o_part, lse_part, w1 > w0 ? w1 - w0 : 0, slot, h, heads,
-               out + ((int64_t)b * heads + h) * kVDim, lse ? lse + (int64_t)b * heads + h : nullptr);
+  combine_row(o_part, lse_part, w1 > w0 ? w1 - w0 : 0, slot, h, heads,
+              out + ((int64_t)b * heads + h) * kVDim, lse ? lse + (int64_t)b * heads + h : nullptr);
 }
 
 cudaError_t launch_offsets_combine(const float *o_part, const float *lse_part,
                                    const int32_t *offsets, int32_t batch, int32_t heads, void *out,
                                    float *lse, cudaStream_t stream) {
-  dim3 grid(batch, (heads + 3) / 4);
-  offsets_combine_kernel<<<grid, 128, 0, stream>>>(o_part, lse_part, offsets, heads,
-                                                   (__nv_bfloat16 *)out, lse);
+  dim3 grid(batch, heads);
+  offsets_combine_kernel<<<grid, kCombineThreads, 0, stream>>>(o_part, lse_part, offsets, heads,
+                                                               (__nv_bfloat16 *)out, lse);
   return cudaGetLastError();
 }
 
