@@ -33,6 +33,15 @@ __device__ __forceinline__ void report(int32_t *dev_status, int32_t code) {
 // the segment of request b in range p uses slot 2p if R_p >= U_b (the range
 // starts inside or at b) and 2p+1 otherwise.
 // ---------------------------------------------------------------------------
+// The first kSegCache segments of every range, written by the planner so that
+// a worker learns its work with one memory round trip: request b, tokens
+// [t0, t1), and the partial slot (-1: the request is not split, the segment
+// writes the output directly).  Later segments are found by walking the plan.
+constexpr int kSegCache = 4;
+struct SegRec {
+  int32_t b, t0, t1, slot;
+};
+
 struct PlanHeader {
   int32_t total_units;  // U
   int32_t num_ranges;   // P (0 when U == 0)
@@ -50,11 +59,13 @@ struct PlanHeader {
 //   int32 unit_prefix[B + 1]  U_b
 //   int32 range_first[P_max]  first request with units in range p
 //   int32 counters[B * 2]     split arrival counters (left at zero)
+//   int32 seg_count[P_max]    segments of range p (0 for p >= P)
+//   SegRec seg_rec[P_max][kSegCache]
 //   fp32 lse_part[2 * P_max * H]
 //   fp32 o_part[2 * P_max][512 / 4][H][4]   (one partial's heads of four
 //                                            dims are contiguous)
 struct WorkspaceLayout {
-  size_t seq_len, unit_prefix, range_first, counters, lse_part, o_part, total;
+  size_t seq_len, unit_prefix, range_first, counters, seg_count, seg_rec, lse_part, o_part, total;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -66,6 +77,8 @@ __host__ __device__ inline WorkspaceLayout workspace_layout(int batch, int heads
   w.unit_prefix = o;  o = align256(o + sizeof(int32_t) * ((size_t)batch + 1));
   w.range_first = o;  o = align256(o + sizeof(int32_t) * ((size_t)max_ranges + 1));
   w.counters = o;     o = align256(o + sizeof(int32_t) * 2 * (size_t)batch);
+  w.seg_count = o;    o = align256(o + sizeof(int32_t) * (size_t)max_ranges);
+  w.seg_rec = o;      o = align256(o + sizeof(SegRec) * kSegCache * (size_t)max_ranges);
   w.lse_part = o;     o = align256(o + sizeof(float) * 2 * (size_t)max_ranges * heads);
   w.o_part = o;       o = align256(o + sizeof(float) * 2 * (size_t)max_ranges * heads * kVDim);
   w.total = o;
@@ -78,6 +91,8 @@ struct PlanView {
   const int32_t *unit_prefix;
   const int32_t *range_first;
   int32_t *counters;
+  const int32_t *seg_count;
+  const SegRec *seg_rec;
   float *lse_part;
   float *o_part;
 };
@@ -91,6 +106,8 @@ __host__ __device__ inline PlanView plan_view(void *ws, int batch, int heads, in
   v.unit_prefix = (const int32_t *)(b + l.unit_prefix);
   v.range_first = (const int32_t *)(b + l.range_first);
   v.counters = (int32_t *)(b + l.counters);
+  v.seg_count = (const int32_t *)(b + l.seg_count);
+  v.seg_rec = (const SegRec *)(b + l.seg_rec);
   v.lse_part = (float *)(b + l.lse_part);
   v.o_part = (float *)(b + l.o_part);
   return v;

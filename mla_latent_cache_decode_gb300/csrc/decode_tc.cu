@@ -34,8 +34,8 @@
 // adds TMA instructions on the producer's critical path and, at launch, a
 // burst that delays every CTA's first tiles.)
 //
-// Warp roles: warp 0 loads the own parts; warp 3
-// loads Q's other half per segment and the other parts; warps 1 and 8 issue
+// Warp roles: warp 0 loads the own parts; warp 3 loads the other parts;
+// warp 9 loads every segment's Q; warps 1 and 8 issue
 // the S MMAs of even and odd tiles (warp 1 owns the tensor memory
 // allocation); warp 2 issues the P V MMAs;
 // warps 4-7 (one thread per head) run the online softmax with lazy rescaling
@@ -56,7 +56,7 @@ constexpr int kSlots = 2;                  // slots per part
 constexpr int kVHalf = 256;                // output dims per CTA
 constexpr int kChunkBytes = kTile * 128;   // one 64-dim, 64-token SW128 chunk: 8 KB
 constexpr int kQChunkBytes = 128 * 128;    // one 64-dim chunk of Q for 128 heads: 16 KB
-constexpr int kThreads = 288;              // 9 warps
+constexpr int kThreads = 320;              // 10 warps
 constexpr int kSoftmaxThreads = 128;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;  // S buffers at kColS + 64 * (g & 1)
@@ -89,6 +89,9 @@ struct __align__(1024) Smem {
   int abort;
 };
 
+static_assert(sizeof(((Smem *)0)->own) == 4 * kQChunkBytes,
+              "the first segment's Q own dims are staged in the own ring");
+
 // Tensor maps over the cache viewed as [rows = NB*BS][576]: 3-D views
 // {64 columns, rows, 9 chunks} (chunk stride 128 B) fetch several 64-dim
 // chunks of 64 rows in one box, laid out chunk after chunk; the 2-D view
@@ -112,29 +115,44 @@ struct Params {
   int32_t *dev_status;
 };
 
-// Segments of range p, in plan order: request b, tokens [t0, t1).
+// Segments of range p, in plan order: request b, tokens [t0, t1), partial
+// slot (-1: the request is not split).  The first kSegCache come from the
+// plan's records (one memory round trip); later ones, for ranges that cross
+// many short requests, by walking the plan on from the last request.
 struct SegIter {
   PlanView v;
-  int32_t batch, U, P, r0, r1, b;
-  __device__ void init(const PlanView &pv, int32_t batch_, int32_t p) {
+  int32_t batch, p, n, idx, b;
+  __device__ void init(const PlanView &pv, int32_t batch_, int32_t p_) {
     v = pv;
     batch = batch_;
-    U = v.hdr->total_units;
-    P = v.hdr->num_ranges;
-    r0 = range_begin(p, U, P);
-    r1 = range_begin(p + 1, U, P);
-    b = v.range_first[p] - 1;
+    p = p_;
+    n = v.seg_count[p];
+    idx = 0;
+    b = -1;
   }
-  __device__ bool next(int32_t &t0, int32_t &t1, bool &split, int32_t &Ub) {
+  __device__ bool next(int32_t &t0, int32_t &t1, int32_t &slot) {
+    if (idx >= n) return false;
+    if (idx < kSegCache) {
+      const SegRec r = v.seg_rec[(int64_t)p * kSegCache + idx];
+      ++idx;
+      b = r.b;
+      t0 = r.t0;
+      t1 = r.t1;
+      slot = r.slot;
+      return true;
+    }
+    const int32_t U = v.hdr->total_units, P = v.hdr->num_ranges;
+    const int32_t r0 = range_begin(p, U, P), r1 = range_begin(p + 1, U, P);
     for (++b; b < batch; ++b) {
-      Ub = v.unit_prefix[b];
+      const int32_t Ub = v.unit_prefix[b];
       if (Ub >= r1) return false;
       const int32_t Ue = v.unit_prefix[b + 1];
       const int32_t u0 = max(r0, Ub), u1 = min(r1, Ue);
       if (u0 >= u1) continue;
       t0 = (u0 - Ub) * kTile;
       t1 = min((u1 - Ub) * kTile, v.seq_len[b]);
-      split = range_of(Ub, U, P) != range_of(Ue - 1, U, P);
+      slot = range_of(Ub, U, P) != range_of(Ue - 1, U, P) ? partial_slot(p, U, P, Ub) : -1;
+      ++idx;
       return true;
     }
     return false;
@@ -198,8 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
 
-  const int32_t P = v.hdr->num_ranges;
-  const bool active = pair < P;
+  const bool active = v.seg_count[pair] > 0;  // ranges past the plan's count have none
   const int own0 = half * 4;        // first own 64-dim chunk (of the 8 kv_c chunks)
   const int oth0 = (1 - half) * 4;  // first other chunk
   const int BS = prm.block_size;
@@ -215,9 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t policy = policy_evict_normal();
       SegIter it;
       it.init(v, prm.batch, pair);
-      int32_t t0, t1, Ub;
-      bool split;
-      uint32_t g = 0, seg = 0;
+      int32_t t0, t1, slot_p;
+      uint32_t g = 0;
       const int box_rows = BS < kTile ? BS : kTile;
       const uint32_t box_bytes = (uint32_t)(box_rows * 128);
       const int64_t nb = prm.num_blocks;
@@ -228,11 +244,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int32_t *tab = &s.tab[own_role ? 0 : 1][0][0];
       SegIter fc;
       fc.init(v, prm.batch, pair);
-      int32_t fc_t = 0, fc_t1 = 0, fc_Ub;
-      bool fc_split, fc_more = true;
+      int32_t fc_t = 0, fc_t1 = 0, fc_slot;
+      bool fc_more = true;
       uint32_t fc_g = 0;
       auto fetch_next = [&]() {  // entries of the next tile (if any), as one group
-        while (fc_more && fc_t >= fc_t1) fc_more = fc.next(fc_t, fc_t1, fc_split, fc_Ub);
+        while (fc_more && fc_t >= fc_t1) fc_more = fc.next(fc_t, fc_t1, fc_slot);
         if (fc_more) {
           const int32_t *row = prm.block_table + (int64_t)fc.b * prm.max_blocks_per_seq;
           const int nbx = (min(kTile, fc_t1 - fc_t) + box_rows - 1) / box_rows;
@@ -250,41 +266,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         prefetch_tmap(&maps.kv5);
         prefetch_tmap(&maps.kv1);
-        prefetch_tmap(&maps.q);
       }
       bool ok = true;
-      while (ok && it.next(t0, t1, split, Ub)) {
-        if (!own_role) {
-          // Q of request b, once the previous segment's S MMAs are done with
-          // it: first its own 256 dims (and rope) into the Q buffers, from
-          // where the even S issuer copies the own dims into tensor memory
-          // (tcgen05.cp), then, once copied, its other 256 dims.
-          if (!mbar_wait(smem_u32(&s.q_free), (seg & 1u) ^ 1u, abort_flag, kWaitBudgetNs)) {
-            set_abort(s, prm.dev_status);
-            break;
-          }
-          mbar_arrive_expect_tx(smem_u32(&s.qown_full), 5 * kQChunkBytes);
-          for (int c = 0; c < 4; ++c)
-            tma_load_2d(smem_u32(s.q_other[c]), &maps.q, 64 * (own0 + c), it.b * kHeads,
-                        smem_u32(&s.qown_full));
-          tma_load_2d(smem_u32(s.q_rope), &maps.q, 512, it.b * kHeads, smem_u32(&s.qown_full));
-          {  // the next segment's Q rows into L2 meanwhile
-            SegIter nx = it;
-            int32_t a0, a1, aU;
-            bool asplit;
-            if (nx.next(a0, a1, asplit, aU))
-              for (int c = 0; c < 9; ++c) tma_prefetch_2d(&maps.q, 64 * c, nx.b * kHeads);
-          }
-          if (!mbar_wait(smem_u32(&s.q_tmem), seg & 1u, abort_flag, kWaitBudgetNs)) {
-            set_abort(s, prm.dev_status);
-            break;
-          }
-          mbar_arrive_expect_tx(smem_u32(&s.q_full), 4 * kQChunkBytes);
-          for (int c = 0; c < 4; ++c)
-            tma_load_2d(smem_u32(s.q_other[c]), &maps.q, 64 * (oth0 + c), it.b * kHeads,
-                        smem_u32(&s.q_full));
-        }
-        ++seg;
+      while (ok && it.next(t0, t1, slot_p)) {
         for (int32_t tt = t0; tt < t1; tt += kTile, ++g) {
           fetch_next();
           // this tile's entries (and those of the tile kOtherAhead later) have landed
@@ -306,6 +290,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int slot = g % kSlots;
           const uint32_t par = ((g / kSlots) & 1u) ^ 1u;
           if (own_role) {
+            // the first segment's Q own dims are staged in the own ring: its
+            // first loads wait until they have been copied to tensor memory
+            if (g == 0 && !mbar_wait(smem_u32(&s.q_tmem), 0, abort_flag, kWaitBudgetNs)) {
+              set_abort(s, prm.dev_status);
+              ok = false;
+              break;
+            }
             if (!mbar_wait(smem_u32(&s.own_empty[slot]), par, abort_flag, kWaitBudgetNs)) {
               set_abort(s, prm.dev_status);
               ok = false;
@@ -373,10 +364,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kSlots; ++i)
           (void)mbar_wait(smem_u32(own_role ? &s.own_full[i] : &s.other_full[i]), 0, nullptr,
                           kDrainBudgetNs);
-        if (!own_role) {
-          (void)mbar_wait(smem_u32(&s.qown_full), 0, nullptr, kDrainBudgetNs);
-          (void)mbar_wait(smem_u32(&s.q_full), 0, nullptr, kDrainBudgetNs);
-        }
       }
     }
   } else if (warp == 1 || warp == 8) {
@@ -391,8 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (active && elect_one_sync()) {
       SegIter it;
       it.init(v, prm.batch, pair);
-      int32_t t0, t1, Ub;
-      bool split;
+      int32_t t0, t1, slot_p;
       uint32_t g = 0, seg = 0;
       const uint32_t id = idesc_bf16_f32(128, kTile, 0);
       // descriptors of slot 0 / chunk 0; chunks, slots and k-steps add their
@@ -401,24 +387,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t d_own = smem_desc(smem_u32(s.own[0][0]), 16, 1024, kSwizzle128B);
       const uint64_t d_oth = smem_desc(smem_u32(s.other[0][0]), 16, 1024, kSwizzle128B);
       const uint64_t d_q = smem_desc(smem_u32(s.q_other[0]), 16, 1024, kSwizzle128B);
+      const uint64_t d_qstart = smem_desc(smem_u32(s.own[0][0]), 16, 1024, kSwizzle128B);
       const uint64_t d_rope = smem_desc(smem_u32(s.q_rope), 16, 1024, kSwizzle128B);
       const uint32_t a_q = tmem + kColQ;
       bool ok = true;
-      while (ok && it.next(t0, t1, split, Ub)) {
+      while (ok && it.next(t0, t1, slot_p)) {
         if (!mbar_wait(smem_u32(&s.qown_full), seg & 1u, abort_flag, kWaitBudgetNs)) {
           set_abort(s, prm.dev_status);
           break;
         }
         if (par == 0) {
-          // Q[:, own 256 dims] (staged in the Q buffers) into tensor memory:
-          // 16 copies of 128 rows x 16 dims, addressed like the A operand
+          // Q[:, own 256 dims] into tensor memory: 16 copies of 128 rows x 16
+          // dims, addressed like the A operand.  Staged in the (still empty)
+          // own ring for the first segment, in the Q buffers afterwards.
+          const uint64_t d_src = seg == 0 ? d_qstart : d_q;
           tc_fence_after();
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               tmem_cp_128x256b(a_q + c * 32 + kk * 8,
-                               d_q + (uint64_t)((c * kQChunkBytes + kk * 32) >> 4));
+                               d_src + (uint64_t)((c * kQChunkBytes + kk * 32) >> 4));
           mma_commit(smem_u32(&s.q_tmem));
         }
         if (!mbar_wait(smem_u32(&s.q_tmem), seg & 1u, abort_flag, kWaitBudgetNs) ||
@@ -487,13 +476,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (active && elect_one_sync()) {
       SegIter it;
       it.init(v, prm.batch, pair);
-      int32_t t0, t1, Ub;
-      bool split;
+      int32_t t0, t1, slot_p;
       uint32_t g = 0;
       const uint32_t id_pv = idesc_bf16_f32(128, kVHalf, 1);
       const uint64_t d_own = smem_desc(smem_u32(s.own[0][0]), kChunkBytes, 1024, kSwizzle128B);
       bool ok = true;
-      while (ok && it.next(t0, t1, split, Ub)) {
+      while (ok && it.next(t0, t1, slot_p)) {
         for (int32_t tt = t0; tt < t1; tt += kTile, ++g) {
           const int n = min(kTile, t1 - tt);
           const int slot = g % kSlots;
@@ -517,6 +505,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(smem_u32(&s.fin_pv), 0, nullptr, kWaitBudgetNs))
         report(prm.dev_status, MLA_ERR_DEVICE_TIMEOUT);
     }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ Q loader
+    // Q of every segment's request, once the previous segment's S MMAs are
+    // done with the Q buffers: first its own 256 dims (and rope), from where
+    // the even S issuer copies the own dims into tensor memory (tcgen05.cp),
+    // then, once copied, its other 256 dims.  A warp of its own, so that the
+    // tile loads never wait behind Q.
+    if (active && elect_one_sync()) {
+      SegIter it;
+      it.init(v, prm.batch, pair);
+      int32_t t0, t1, slot_p;
+      uint32_t seg = 0;
+      prefetch_tmap(&maps.q);
+      while (it.next(t0, t1, slot_p)) {
+        if (!mbar_wait(smem_u32(&s.q_free), (seg & 1u) ^ 1u, abort_flag, kWaitBudgetNs)) {
+          set_abort(s, prm.dev_status);
+          break;
+        }
+        // own dims: into the own ring for the first segment (empty until the
+        // copy is done, so Q's other dims need not wait), else the Q buffers
+        uint8_t *own_stage = seg == 0 ? s.own[0][0] : s.q_other[0];
+        mbar_arrive_expect_tx(smem_u32(&s.qown_full), 5 * kQChunkBytes);
+        for (int c = 0; c < 4; ++c)
+          tma_load_2d(smem_u32(own_stage + c * kQChunkBytes), &maps.q, 64 * (own0 + c),
+                      it.b * kHeads, smem_u32(&s.qown_full));
+        tma_load_2d(smem_u32(s.q_rope), &maps.q, 512, it.b * kHeads, smem_u32(&s.qown_full));
+        {  // the next segment's Q rows into L2 meanwhile
+          SegIter nx = it;
+          int32_t a0, a1, aslot;
+          if (nx.next(a0, a1, aslot))
+            for (int c = 0; c < 9; ++c) tma_prefetch_2d(&maps.q, 64 * c, nx.b * kHeads);
+        }
+        if (seg > 0 && !mbar_wait(smem_u32(&s.q_tmem), seg & 1u, abort_flag, kWaitBudgetNs)) {
+          set_abort(s, prm.dev_status);
+          break;
+        }
+        mbar_arrive_expect_tx(smem_u32(&s.q_full), 4 * kQChunkBytes);
+        for (int c = 0; c < 4; ++c)
+          tma_load_2d(smem_u32(s.q_other[c]), &maps.q, 64 * (oth0 + c), it.b * kHeads,
+                      smem_u32(&s.q_full));
+        ++seg;
+      }
+      if (s.abort) {  // let the last issued loads land before exit
+        (void)mbar_wait(smem_u32(&s.qown_full), 0, nullptr, kDrainBudgetNs);
+        (void)mbar_wait(smem_u32(&s.q_full), 0, nullptr, kDrainBudgetNs);
+      }
+    }
   } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ softmax / epilogue
     const int q4 = warp & 3;              // TMEM lane quadrant of this warp
@@ -536,17 +571,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (active) {
       SegIter it;
       it.init(v, prm.batch, pair);
-      int32_t t0, t1, Ub;
-      bool split;
+      int32_t t0, t1, slot_p;
       uint32_t g = 0;  // tiles so far
       bool ok = true;
-      bool have = it.next(t0, t1, split, Ub);
+      bool have = it.next(t0, t1, slot_p);
       while (ok && have) {
         const int b = it.b;
         SegIter nx = it;  // the segment after this one, if any
-        int32_t nt0, nt1, nUb;
-        bool nsplit;
-        const bool have_next = nx.next(nt0, nt1, nsplit, nUb);
+        int32_t nt0, nt1, nslot;
+        const bool have_next = nx.next(nt0, nt1, nslot);
 
         float m_used = -INFINITY, l = 0.f;
         for (int32_t tt = t0; tt < t1; tt += kTile, ++g) {
@@ -643,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const float inv = 1.f / l;
         const float lse_val = (m_used + log2f(l)) * 0.69314718055994531f;
-        if (!split) {
+        if (slot_p < 0) {
           uint4 *dst = (uint4 *)(prm.out + ((int64_t)b * kHeads + h) * kVDim + half * kVHalf);
 #pragma unroll 1
           for (int c = 0; c < kVHalf; c += 32) {
@@ -663,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // partials are stored as [slot][dim / 4][head][4]: a warp's 32 heads
           // of four dims are 512 contiguous bytes, so every float4 store
           // coalesces (head-major rows, one per thread, cost a line per lane)
-          const int slot = partial_slot(pair, it.U, it.P, Ub);
+          const int slot = slot_p;
           float4 *dst = reinterpret_cast<float4 *>(v.o_part) +
                         ((int64_t)slot * (kVDim / 4) + half * (kVHalf / 4)) * kHeads + h;
 #pragma unroll 1
@@ -684,8 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         it = nx;
         t0 = nt0;
         t1 = nt1;
-        split = nsplit;
-        Ub = nUb;
+        slot_p = nslot;
         have = have_next;
       }
     }

@@ -81,6 +81,31 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
     }
     range_first[p] = lo;
   }
+  __syncthreads();  // range_first, prefix and the clamped lengths are visible to the block
+  // the first kSegCache segments of every range (see SegRec)
+  int32_t *seg_count = const_cast<int32_t *>(v.seg_count);
+  SegRec *seg_rec = const_cast<SegRec *>(v.seg_rec);
+  for (int p = tid; p < max_ranges; p += kPlanThreads) {
+    int32_t n = 0;
+    if (p < P) {
+      const int32_t r0 = range_begin(p, U, P), r1 = range_begin(p + 1, U, P);
+      for (int b = range_first[p]; b < batch && prefix[b] < r1; ++b) {
+        const int32_t Ub = prefix[b], Ue = prefix[b + 1];
+        const int32_t u0 = max(r0, Ub), u1 = min(r1, Ue);
+        if (u0 >= u1) continue;
+        if (n < kSegCache) {
+          SegRec r;
+          r.b = b;
+          r.t0 = (u0 - Ub) * unit_tokens;
+          r.t1 = min((u1 - Ub) * unit_tokens, seq_out[b]);
+          r.slot = range_of(Ub, U, P) != range_of(Ue - 1, U, P) ? partial_slot(p, U, P, Ub) : -1;
+          seg_rec[(int64_t)p * kSegCache + n] = r;
+        }
+        ++n;
+      }
+    }
+    seg_count[p] = n;
+  }
   if (tid == 0) {
     PlanHeader *h = const_cast<PlanHeader *>(v.hdr);
     h->total_units = U;
