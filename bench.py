@@ -43,6 +43,22 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
+def reduce_max(x, world, device=None):
+    """Max of a per-rank float over all ranks (the slowest rank sets the time)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput_gbs(world, bytes_per_rank_step, ms_per_step):
+    """Whole-job GB/s: every rank processes its own replica of the workload."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -125,11 +141,49 @@ def build_device_workload(w, device):
 
 
 def algorithmic_bytes_per_layer(w):
+    """(cache rows read, decode kernel's algorithmic bytes = cache + q, out written,
+    appended rows written) per layer."""
     cache = sum(w.seq_lens) * ROW_BYTES
     q = w.batch * 128 * mi.ROW * 2
     out = w.batch * 128 * 512 * 2
     append = w.batch * ROW_BYTES if w.append else 0
-    return cache, q + out + cache, append
+    return cache, cache + q, out, append
+
+
+KERNEL_SOURCES = ("mla_latent_cache_decode_gb300/csrc/decode_tc.cu",
+                  "mla_latent_cache_decode_gb300/csrc/sm100.cuh",
+                  "mla_latent_cache_decode_gb300/csrc/common.cuh", "include/mla.h")
+TRAFFIC_PROFILE = "profiles/decode_tc_dp_rank_layer_b20x4096_dram.md"
+
+
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(w):
+    """DRAM bytes per decode launch from the committed ncu capture, if it was taken
+    on this workload's layer shape with the kernel as it is now; else None."""
+    path = os.path.join(ROOT, TRAFFIC_PROFILE)
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.startswith("- "):
+                k, v = line[2:].split(":", 1)
+                fields[k.strip()] = v.strip().strip("`")
+    base = w.name.split("_first")[0]  # a --layers run has the same per-layer launch
+    if fields.get("workload") != base or fields.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    try:
+        return int(fields["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 def algorithmic_flops_per_layer(w):
@@ -164,12 +218,15 @@ def run_mine(args, w, rank, world, local_rank):
             if w.append:
                 mla.mla_cache_append(d["kv_new"], W["slots"], d["cache"], dev_status=status,
                                      stream=sh)
+            # mla_decode_planned, as its two launches so that the decode
+            # kernel can be timed on its own
             if timing_events is not None:
                 timing_events[l][0].record(stream)
-            mla.mla_decode_planned(d["q"], d["cache"], W["bt"], W["seq"], scale, W["outs"][l],
+            mla.mla_decode_partial(d["q"], d["cache"], W["bt"], W["seq"], scale, W["outs"][l],
                                    W["lses"][l], workspace=ws, dev_status=status, stream=sh)
             if timing_events is not None:
                 timing_events[l][1].record(stream)
+            mla.mla_combine_planned(ws, w.batch, W["outs"][l], W["lses"][l], stream=sh)
 
     launches_per_step = 1 + L * ((1 if w.append else 0) + 2)
 
@@ -209,12 +266,7 @@ def run_mine(args, w, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop() if rank == 0 else None
-    ms_total = e0.elapsed_time(e1)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_total], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = reduce_max(e0.elapsed_time(e1), world, device)
     ms_step = ms_total / args.steps
     assert int(status.item()) == 0, f"device status {int(status.item())}"
 
@@ -271,12 +323,8 @@ def run_mine(args, w, rank, world, local_rank):
         e2e_step()
     a1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max(a0.elapsed_time(a1), (time.perf_counter() - t0) * 1e3) / esteps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_max(max(a0.elapsed_time(a1), (time.perf_counter() - t0) * 1e3) / esteps,
+                        world, device)
     assert int(status.item()) == 0
 
     if rank != 0:
@@ -285,12 +333,12 @@ def run_mine(args, w, rank, world, local_rank):
             dist.destroy_process_group()
         return None
 
-    cache_b, decode_b, append_b = algorithmic_bytes_per_layer(w)
+    cache_b, decode_b, out_b, append_b = algorithmic_bytes_per_layer(w)
     step_cache_bytes = cache_b * L
-    value = world * step_cache_bytes / (ms_step * 1e-3) / 1e9
+    value = job_throughput_gbs(world, step_cache_bytes, ms_step)
     hbm_peak, tf_peak, src = measured_peaks()
     achieved = decode_b / (decode_ms * 1e-3) / 1e9
-    step_bytes = (decode_b + append_b) * L
+    step_bytes = (decode_b + out_b + append_b) * L
     roofline_step_us = max(step_bytes / (hbm_peak * 1e9),
                            algorithmic_flops_per_layer(w) * L / (tf_peak * 1e12)) * 1e6
     result = {
@@ -306,12 +354,13 @@ def run_mine(args, w, rank, world, local_rank):
                    "cuda_graph": graph is not None,
                    "parallelism": "dp-attention rank per GPU; replicas only"},
         "step_roofline_frac": round(roofline_step_us / (ms_step * 1e3), 4),
-        "roofline": {"bound": "hbm", "kernel": "mla decode", "achieved": round(achieved, 1),
-                     "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                     "peak_source": src, "traffic": None,
+        "roofline": {"bound": "hbm", "kernel": "decode_tc_kernel (mla_decode_partial)",
+                     "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "peak_source": src,
+                     "traffic": measured_traffic(w),
                      "algorithmic_bytes_per_launch": decode_b,
                      "launch_us": round(decode_ms * 1e3, 2)},
-        "e2e": {"value": round(world * step_cache_bytes / (e2e_ms * 1e-3) / 1e9, 2),
+        "e2e": {"value": round(job_throughput_gbs(world, step_cache_bytes, e2e_ms), 2),
                 "unit": "GB/s", "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
@@ -413,11 +462,16 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="run only the first N layers of the workload (for profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     rank, world, local_rank = dist_env()
     w = mi.workload(args.config)
+    if args.layers and args.layers < w.layers:
+        import dataclasses
+        w = dataclasses.replace(w, layers=args.layers, name=f"{w.name}_first{args.layers}")
     if args.impl == "reference":
         res = run_reference(args, w, rank, world)
     else:

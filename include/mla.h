@@ -169,6 +169,26 @@ mla_status_t mla_decode_planned(const void *q, const void *cache, int64_t num_bl
                                 size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /*
+ * mla_decode_partial / mla_combine_planned — the two launches of
+ * mla_decode_planned, for callers that want to place or time them apart.
+ * mla_decode_partial runs the decode kernel over the plan's token ranges:
+ * requests that lie in one range get their out (and lse) written; requests
+ * spread over several ranges leave one fp32 partial result per range in the
+ * workspace.  mla_combine_planned then merges those partials into out / lse
+ * (requests that were not split are left as they are).  Same arguments and
+ * requirements as mla_decode_planned; the workspace must not be touched
+ * between the two calls.  mla_decode_planned == partial, then combine.
+ */
+mla_status_t mla_decode_partial(const void *q, const void *cache, int64_t num_blocks,
+                                int32_t block_size, const int32_t *block_table,
+                                int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                int32_t batch, int32_t num_heads, int32_t max_seq_len,
+                                float softmax_scale, void *out, float *lse, void *workspace,
+                                size_t workspace_bytes, int32_t *dev_status, void *stream);
+mla_status_t mla_combine_planned(void *workspace, size_t workspace_bytes, int32_t batch,
+                                 int32_t num_heads, void *out, float *lse, void *stream);
+
+/*
  * mla_combine — merge split-KV partial results (flash-decoding).
  *
  * Partial w (one token range of one request) holds o_partial[w] = its own

@@ -28,7 +28,7 @@ STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARGUMENT", 2: "MLA_ERR_UNSUPPORTED",
           6: "MLA_ERR_DEVICE_TIMEOUT"}
 EXPORTED = ("mla_status_string", "mla_last_error_detail", "mla_abi_version", "mla_cache_append",
             "mla_decode_workspace_size", "mla_decode_plan", "mla_decode", "mla_decode_planned",
-            "mla_combine", "mla_decode_noalloc")
+            "mla_combine", "mla_decode_noalloc", "mla_decode_partial", "mla_combine_planned")
 
 
 class MlaError(RuntimeError):
@@ -62,6 +62,10 @@ def _load():
     lib.mla_decode.restype = ctypes.c_int
     lib.mla_decode_planned.argtypes = dec
     lib.mla_decode_planned.restype = ctypes.c_int
+    lib.mla_decode_partial.argtypes = dec
+    lib.mla_decode_partial.restype = ctypes.c_int
+    lib.mla_combine_planned.argtypes = [P, sz, i32, i32, P, P, P]
+    lib.mla_combine_planned.restype = ctypes.c_int
     lib.mla_combine.argtypes = [P, P, P, i32, i32, P, P, P]
     lib.mla_combine.restype = ctypes.c_int
     lib.mla_decode_noalloc.argtypes = [P, P, i64, i32, P, i32, P, i32, i32, i32, f32, P, P, P, P]
@@ -194,6 +198,25 @@ def mla_decode_planned(q, cache, block_table, seq_lens, softmax_scale, out, lse=
     """mla_decode reusing the plan mla_decode_plan wrote into `workspace`."""
     return _decode(get_lib().mla_decode_planned, q, cache, block_table, seq_lens, softmax_scale, out,
                    lse, workspace, max_seq_len, dev_status, stream)
+
+
+def mla_decode_partial(q, cache, block_table, seq_lens, softmax_scale, out, lse=None,
+                       workspace=None, max_seq_len=None, dev_status=None, stream=None):
+    """The decode kernel of mla_decode_planned alone (split requests leave partials)."""
+    return _decode(get_lib().mla_decode_partial, q, cache, block_table, seq_lens, softmax_scale,
+                   out, lse, workspace, max_seq_len, dev_status, stream)
+
+
+def mla_combine_planned(workspace, batch, out, lse=None, num_heads=NUM_HEADS, stream=None):
+    """Merge the partials mla_decode_partial left in `workspace` into out / lse."""
+    import torch
+    _need(out, torch.bfloat16, 3, "out")
+    if lse is not None:
+        _need(lse, torch.float32, 2, "lse")
+    _check(get_lib().mla_combine_planned(_ptr(workspace),
+                                         workspace.numel() * workspace.element_size(), int(batch),
+                                         num_heads, _ptr(out), _ptr(lse), _stream(stream)))
+    return out
 
 
 def mla_combine(o_partial, lse_partial, split_offsets, out, lse=None, stream=None):

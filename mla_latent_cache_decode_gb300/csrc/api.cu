@@ -181,7 +181,7 @@ mla_status_t mla_decode_plan(const int32_t *seq_lens, int32_t batch, int32_t num
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "plan launch");
 }
 
-mla_status_t mla_decode_planned(const void *q, const void *cache, int64_t num_blocks,
+mla_status_t mla_decode_partial(const void *q, const void *cache, int64_t num_blocks,
                                 int32_t block_size, const int32_t *block_table,
                                 int32_t max_blocks_per_seq, const int32_t *seq_lens,
                                 int32_t batch, int32_t num_heads, int32_t max_seq_len,
@@ -192,14 +192,42 @@ mla_status_t mla_decode_planned(const void *q, const void *cache, int64_t num_bl
                                      max_blocks_per_seq, seq_lens, batch, num_heads, max_seq_len,
                                      softmax_scale, out, lse, workspace, workspace_bytes);
   if (s != MLA_OK || batch == 0) return s;
-  const int ranges = max_ranges_current();
-  cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e = launch_decode_tc(q, cache, num_blocks, block_size, block_table,
                                    max_blocks_per_seq, batch, softmax_scale, out, lse, workspace,
-                                   ranges, dev_status, st);
-  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  e = launch_plan_combine(workspace, batch, num_heads, ranges, out, lse, st);
+                                   max_ranges_current(), dev_status, (cudaStream_t)stream);
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e, "decode launch");
+}
+
+mla_status_t mla_combine_planned(void *workspace, size_t workspace_bytes, int32_t batch,
+                                 int32_t num_heads, void *out, float *lse, void *stream) {
+  g_detail.clear();
+  if (batch < 0) return fail(MLA_ERR_INVALID_ARGUMENT, "batch < 0");
+  if (num_heads != kHeads) return fail(MLA_ERR_UNSUPPORTED, "num_heads must be %d", kHeads);
+  if (batch == 0) return MLA_OK;
+  if (!workspace || !out) return fail(MLA_ERR_INVALID_ARGUMENT, "null pointer");
+  if (!aligned(workspace, 256) || !aligned(out, 16) || (lse && !aligned(lse, 4)))
+    return fail(MLA_ERR_INVALID_ARGUMENT, "workspace / out / lse alignment");
+  const size_t need = mla_decode_workspace_size(batch, num_heads);
+  if (need == 0) return fail(MLA_ERR_CUDA, "cannot query the current device");
+  if (workspace_bytes < need)
+    return fail(MLA_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu", workspace_bytes, need);
+  cudaError_t e = launch_plan_combine(workspace, batch, num_heads, max_ranges_current(), out, lse,
+                                      (cudaStream_t)stream);
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "combine launch");
+}
+
+mla_status_t mla_decode_planned(const void *q, const void *cache, int64_t num_blocks,
+                                int32_t block_size, const int32_t *block_table,
+                                int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                int32_t batch, int32_t num_heads, int32_t max_seq_len,
+                                float softmax_scale, void *out, float *lse, void *workspace,
+                                size_t workspace_bytes, int32_t *dev_status, void *stream) {
+  mla_status_t s = mla_decode_partial(q, cache, num_blocks, block_size, block_table,
+                                      max_blocks_per_seq, seq_lens, batch, num_heads, max_seq_len,
+                                      softmax_scale, out, lse, workspace, workspace_bytes,
+                                      dev_status, stream);
+  if (s != MLA_OK || batch == 0) return s;
+  return mla_combine_planned(workspace, workspace_bytes, batch, num_heads, out, lse, stream);
 }
 
 mla_status_t mla_decode(const void *q, const void *cache, int64_t num_blocks, int32_t block_size,

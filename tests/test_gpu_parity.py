@@ -385,6 +385,31 @@ def test_config4_every_short_request_repeated(mla, q_kind):
         assert torch.equal(lse2, lse), f"repeat {rep} lse"
 
 
+def test_partial_then_combine_equals_planned(mla):
+    """mla_decode_partial + mla_combine_planned is exactly mla_decode_planned."""
+    w = mi.workload(4)
+    dl, host = _device_layer_and_host(w, 0, "sharp")
+    ws = mla.make_workspace(w.batch)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.mla_cache_append(dl["kv_new"], dl["slot_mapping"], dl["cache"], dev_status=status)
+    mla.mla_decode_plan(dl["seq_lens"], dl["block_table"], w.block_size, ws, dev_status=status)
+    outs = []
+    for split_calls in (False, True):
+        out = torch.empty((w.batch, 128, 512), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((w.batch, 128), dtype=torch.float32, device="cuda")
+        args = (dl["q"], dl["cache"], dl["block_table"], dl["seq_lens"], dl["softmax_scale"], out, lse)
+        if split_calls:
+            mla.mla_decode_partial(*args, workspace=ws, dev_status=status)
+            mla.mla_combine_planned(ws, w.batch, out, lse)
+        else:
+            mla.mla_decode_planned(*args, workspace=ws, dev_status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        outs.append((out, lse))
+    assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
+    assert torch.equal(outs[0][1], outs[1][1])
+
+
 def test_config5_mixed_fragmented_sampled(mla):
     w = mi.workload(5)
     bt = mi.make_block_table(mi.rng_for(5, 0, 1), w.seq_lens, w.block_size, w.num_blocks())
