@@ -215,20 +215,19 @@ def run_mine(args, w, rank, world, local_rank):
         mla.mla_decode_plan(W["seq"], W["bt"], w.block_size, ws, dev_status=status, stream=sh)
         for l in range(L):
             d = W["layers"][l]
-            if w.append:
-                mla.mla_cache_append(d["kv_new"], W["slots"], d["cache"], dev_status=status,
-                                     stream=sh)
-            # mla_decode_planned, as its two launches so that the decode
+            # mla_decode_append_planned (the append of this step's row fused
+            # into the decode kernel), as its two launches so that the decode
             # kernel can be timed on its own
             if timing_events is not None:
                 timing_events[l][0].record(stream)
             mla.mla_decode_partial(d["q"], d["cache"], W["bt"], W["seq"], scale, W["outs"][l],
-                                   W["lses"][l], workspace=ws, dev_status=status, stream=sh)
+                                   W["lses"][l], workspace=ws, dev_status=status, stream=sh,
+                                   kv_new=d["kv_new"] if w.append else None)
             if timing_events is not None:
                 timing_events[l][1].record(stream)
             mla.mla_combine_planned(ws, w.batch, W["outs"][l], W["lses"][l], stream=sh)
 
-    launches_per_step = 1 + L * ((1 if w.append else 0) + 2)
+    launches_per_step = 1 + L * 2
 
     for _ in range(args.warmup):
         step()
@@ -286,28 +285,28 @@ def run_mine(args, w, rank, world, local_rank):
     kv_host = [d["kv_new"].cpu().pin_memory() for d in W["layers"]]
     seq_host = W["seq"].cpu().pin_memory()
     bt_host = W["bt"].cpu().pin_memory()
-    slot_host = W["slots"].cpu().pin_memory()
     out_host = [torch.empty_like(o, device="cpu").pin_memory() for o in W["outs"]]
     qd = [torch.empty_like(d["q"]) for d in W["layers"]]
     kvd = [torch.empty_like(d["kv_new"]) for d in W["layers"]]
-    seqd, btd, slotd = (torch.empty_like(W["seq"]), torch.empty_like(W["bt"]),
-                        torch.empty_like(W["slots"]))
-    h2d = sum(t.numel() * t.element_size() for t in q_host + kv_host + [seq_host, bt_host, slot_host])
+    seqd, btd = torch.empty_like(W["seq"]), torch.empty_like(W["bt"])
+    h2d = sum(t.numel() * t.element_size() for t in q_host + kv_host + [seq_host, bt_host])
     d2h = sum(t.numel() * t.element_size() for t in out_host)
 
     def e2e_step():
         seqd.copy_(seq_host, non_blocking=True)
         btd.copy_(bt_host, non_blocking=True)
-        slotd.copy_(slot_host, non_blocking=True)
         mla.mla_decode_plan(seqd, btd, w.block_size, ws, dev_status=status, stream=sh)
         for l in range(L):
             d = W["layers"][l]
             qd[l].copy_(q_host[l], non_blocking=True)
             kvd[l].copy_(kv_host[l], non_blocking=True)
             if w.append:
-                mla.mla_cache_append(kvd[l], slotd, d["cache"], dev_status=status, stream=sh)
-            mla.mla_decode_planned(qd[l], d["cache"], btd, seqd, scale, W["outs"][l],
-                                   W["lses"][l], workspace=ws, dev_status=status, stream=sh)
+                mla.mla_decode_append_planned(qd[l], d["cache"], kvd[l], btd, seqd, scale,
+                                              W["outs"][l], W["lses"][l], workspace=ws,
+                                              dev_status=status, stream=sh)
+            else:
+                mla.mla_decode_planned(qd[l], d["cache"], btd, seqd, scale, W["outs"][l],
+                                       W["lses"][l], workspace=ws, dev_status=status, stream=sh)
             out_host[l].copy_(W["outs"][l], non_blocking=True)
 
     for _ in range(2):

@@ -170,23 +170,45 @@ mla_status_t mla_decode_planned(const void *q, const void *cache, int64_t num_bl
 
 /*
  * mla_decode_partial / mla_combine_planned — the two launches of
- * mla_decode_planned, for callers that want to place or time them apart.
- * mla_decode_partial runs the decode kernel over the plan's token ranges:
- * requests that lie in one range get their out (and lse) written; requests
- * spread over several ranges leave one fp32 partial result per range in the
- * workspace.  mla_combine_planned then merges those partials into out / lse
- * (requests that were not split are left as they are).  Same arguments and
- * requirements as mla_decode_planned; the workspace must not be touched
- * between the two calls.  mla_decode_planned == partial, then combine.
+ * mla_decode_planned (and of mla_decode_append_planned), for callers that want
+ * to place or time them apart.  mla_decode_partial runs the decode kernel over
+ * the plan's token ranges: requests that lie in one range get their out (and
+ * lse) written; requests spread over several ranges leave one fp32 partial
+ * result per range in the workspace.  With kv_new non-null it first stores
+ * each request's new row as mla_decode_append_planned does (the cache is
+ * written then; with kv_new NULL it is only read).  mla_combine_planned then
+ * merges the partials into out / lse (requests that were not split are left
+ * as they are).  Same arguments and requirements as mla_decode_planned; the
+ * workspace must not be touched between the two calls.
  */
-mla_status_t mla_decode_partial(const void *q, const void *cache, int64_t num_blocks,
-                                int32_t block_size, const int32_t *block_table,
-                                int32_t max_blocks_per_seq, const int32_t *seq_lens,
-                                int32_t batch, int32_t num_heads, int32_t max_seq_len,
-                                float softmax_scale, void *out, float *lse, void *workspace,
-                                size_t workspace_bytes, int32_t *dev_status, void *stream);
+mla_status_t mla_decode_partial(const void *q, void *cache, const void *kv_new,
+                                int64_t num_blocks, int32_t block_size,
+                                const int32_t *block_table, int32_t max_blocks_per_seq,
+                                const int32_t *seq_lens, int32_t batch, int32_t num_heads,
+                                int32_t max_seq_len, float softmax_scale, void *out, float *lse,
+                                void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                                void *stream);
 mla_status_t mla_combine_planned(void *workspace, size_t workspace_bytes, int32_t batch,
                                  int32_t num_heads, void *out, float *lse, void *stream);
+
+/*
+ * mla_decode_append_planned — one decode step with its cache append fused in:
+ * stores kv_new[b] (bf16 [batch, 576], the new latent row of request b) at
+ * position seq_lens[b] - 1 of request b, i.e. at cache row
+ * block_table[b][(L-1)/BS] * BS + (L-1) % BS, then decodes over the full
+ * context, all in the decode kernel (requests with seq_lens[b] == 0 store
+ * nothing).  Same result as mla_cache_append with that slot mapping followed
+ * by mla_decode_planned; the cache must be writable.  A block-table entry
+ * outside the pool is reported as MLA_ERR_DEVICE_RANGE and its row is not
+ * stored.  For other slot mappings use mla_cache_append.
+ */
+mla_status_t mla_decode_append_planned(const void *q, void *cache, const void *kv_new,
+                                       int64_t num_blocks, int32_t block_size,
+                                       const int32_t *block_table, int32_t max_blocks_per_seq,
+                                       const int32_t *seq_lens, int32_t batch, int32_t num_heads,
+                                       int32_t max_seq_len, float softmax_scale, void *out,
+                                       float *lse, void *workspace, size_t workspace_bytes,
+                                       int32_t *dev_status, void *stream);
 
 /*
  * mla_combine — merge split-KV partial results (flash-decoding).

@@ -28,7 +28,8 @@ STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARGUMENT", 2: "MLA_ERR_UNSUPPORTED",
           6: "MLA_ERR_DEVICE_TIMEOUT"}
 EXPORTED = ("mla_status_string", "mla_last_error_detail", "mla_abi_version", "mla_cache_append",
             "mla_decode_workspace_size", "mla_decode_plan", "mla_decode", "mla_decode_planned",
-            "mla_combine", "mla_decode_noalloc", "mla_decode_partial", "mla_combine_planned")
+            "mla_combine", "mla_decode_noalloc", "mla_decode_partial", "mla_combine_planned",
+            "mla_decode_append_planned")
 
 
 class MlaError(RuntimeError):
@@ -62,10 +63,14 @@ def _load():
     lib.mla_decode.restype = ctypes.c_int
     lib.mla_decode_planned.argtypes = dec
     lib.mla_decode_planned.restype = ctypes.c_int
-    lib.mla_decode_partial.argtypes = dec
+    lib.mla_decode_partial.argtypes = [P, P, P, i64, i32, P, i32, P, i32, i32, i32, f32, P, P, P,
+                                       sz, P, P]
     lib.mla_decode_partial.restype = ctypes.c_int
     lib.mla_combine_planned.argtypes = [P, sz, i32, i32, P, P, P]
     lib.mla_combine_planned.restype = ctypes.c_int
+    lib.mla_decode_append_planned.argtypes = [P, P, P, i64, i32, P, i32, P, i32, i32, i32, f32,
+                                              P, P, P, sz, P, P]
+    lib.mla_decode_append_planned.restype = ctypes.c_int
     lib.mla_combine.argtypes = [P, P, P, i32, i32, P, P, P]
     lib.mla_combine.restype = ctypes.c_int
     lib.mla_decode_noalloc.argtypes = [P, P, i64, i32, P, i32, P, i32, i32, i32, f32, P, P, P, P]
@@ -200,11 +205,38 @@ def mla_decode_planned(q, cache, block_table, seq_lens, softmax_scale, out, lse=
                    lse, workspace, max_seq_len, dev_status, stream)
 
 
+def _with_kv_new(entry, kv_new, q):
+    import torch
+    if kv_new is not None:
+        _need(kv_new, torch.bfloat16, 2, "kv_new")
+        if tuple(kv_new.shape) != (q.shape[0], ROW_DIM):
+            raise ValueError("kv_new must be [B, 576]")
+
+    def fn(qp, cp, nb, bs, btp, mb, slp, B, H, msl, sc, op, lp, wp, wb, dsp, st):
+        return entry(qp, cp, _ptr(kv_new), nb, bs, btp, mb, slp, B, H, msl, sc, op, lp, wp, wb,
+                     dsp, st)
+    return fn
+
+
 def mla_decode_partial(q, cache, block_table, seq_lens, softmax_scale, out, lse=None,
-                       workspace=None, max_seq_len=None, dev_status=None, stream=None):
-    """The decode kernel of mla_decode_planned alone (split requests leave partials)."""
-    return _decode(get_lib().mla_decode_partial, q, cache, block_table, seq_lens, softmax_scale,
-                   out, lse, workspace, max_seq_len, dev_status, stream)
+                       workspace=None, max_seq_len=None, dev_status=None, stream=None,
+                       kv_new=None):
+    """The decode kernel of mla_decode_planned alone (split requests leave partials);
+    with kv_new, each request's new row is stored first (as mla_decode_append_planned)."""
+    return _decode(_with_kv_new(get_lib().mla_decode_partial, kv_new, q), q, cache, block_table,
+                   seq_lens, softmax_scale, out, lse, workspace, max_seq_len, dev_status, stream)
+
+
+def mla_decode_append_planned(q, cache, kv_new, block_table, seq_lens, softmax_scale, out,
+                              lse=None, workspace=None, max_seq_len=None, dev_status=None,
+                              stream=None):
+    """Store kv_new[b] at position seq_lens[b]-1 of request b, then mla_decode_planned, in
+    one decode kernel (plus the split combine)."""
+    if kv_new is None:
+        raise ValueError("kv_new is required")
+    return _decode(_with_kv_new(get_lib().mla_decode_append_planned, kv_new, q), q, cache,
+                   block_table, seq_lens, softmax_scale, out, lse, workspace, max_seq_len,
+                   dev_status, stream)
 
 
 def mla_combine_planned(workspace, batch, out, lse=None, num_heads=NUM_HEADS, stream=None):

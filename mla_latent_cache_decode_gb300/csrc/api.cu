@@ -26,7 +26,8 @@ int tc_max_pairs();
 cudaError_t launch_decode_tc(const void *q, const void *cache, int64_t num_blocks, int32_t block_size,
                              const int32_t *block_table, int32_t max_blocks_per_seq, int32_t batch,
                              float softmax_scale, void *out, float *lse, void *ws,
-                             int32_t max_ranges, int32_t *dev_status, cudaStream_t stream);
+                             int32_t max_ranges, int32_t *dev_status, cudaStream_t stream,
+                             const void *kv_new = nullptr);
 
 namespace {
 
@@ -181,21 +182,43 @@ mla_status_t mla_decode_plan(const int32_t *seq_lens, int32_t batch, int32_t num
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "plan launch");
 }
 
-mla_status_t mla_decode_partial(const void *q, const void *cache, int64_t num_blocks,
-                                int32_t block_size, const int32_t *block_table,
-                                int32_t max_blocks_per_seq, const int32_t *seq_lens,
-                                int32_t batch, int32_t num_heads, int32_t max_seq_len,
-                                float softmax_scale, void *out, float *lse, void *workspace,
-                                size_t workspace_bytes, int32_t *dev_status, void *stream) {
+mla_status_t mla_decode_partial(const void *q, void *cache, const void *kv_new,
+                                int64_t num_blocks, int32_t block_size,
+                                const int32_t *block_table, int32_t max_blocks_per_seq,
+                                const int32_t *seq_lens, int32_t batch, int32_t num_heads,
+                                int32_t max_seq_len, float softmax_scale, void *out, float *lse,
+                                void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                                void *stream) {
   g_detail.clear();
   mla_status_t s = check_decode_args(q, cache, num_blocks, block_size, block_table,
                                      max_blocks_per_seq, seq_lens, batch, num_heads, max_seq_len,
                                      softmax_scale, out, lse, workspace, workspace_bytes);
   if (s != MLA_OK || batch == 0) return s;
+  if (kv_new && !aligned(kv_new, 16))
+    return fail(MLA_ERR_INVALID_ARGUMENT, "kv_new must be 16-byte aligned");
   cudaError_t e = launch_decode_tc(q, cache, num_blocks, block_size, block_table,
                                    max_blocks_per_seq, batch, softmax_scale, out, lse, workspace,
-                                   max_ranges_current(), dev_status, (cudaStream_t)stream);
+                                   max_ranges_current(), dev_status, (cudaStream_t)stream, kv_new);
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "decode launch");
+}
+
+mla_status_t mla_decode_append_planned(const void *q, void *cache, const void *kv_new,
+                                       int64_t num_blocks, int32_t block_size,
+                                       const int32_t *block_table, int32_t max_blocks_per_seq,
+                                       const int32_t *seq_lens, int32_t batch, int32_t num_heads,
+                                       int32_t max_seq_len, float softmax_scale, void *out,
+                                       float *lse, void *workspace, size_t workspace_bytes,
+                                       int32_t *dev_status, void *stream) {
+  if (!kv_new) {
+    g_detail.clear();
+    return fail(MLA_ERR_INVALID_ARGUMENT, "kv_new is null");
+  }
+  mla_status_t s = mla_decode_partial(q, cache, kv_new, num_blocks, block_size, block_table,
+                                      max_blocks_per_seq, seq_lens, batch, num_heads, max_seq_len,
+                                      softmax_scale, out, lse, workspace, workspace_bytes,
+                                      dev_status, stream);
+  if (s != MLA_OK || batch == 0) return s;
+  return mla_combine_planned(workspace, workspace_bytes, batch, num_heads, out, lse, stream);
 }
 
 mla_status_t mla_combine_planned(void *workspace, size_t workspace_bytes, int32_t batch,
@@ -222,10 +245,10 @@ mla_status_t mla_decode_planned(const void *q, const void *cache, int64_t num_bl
                                 int32_t batch, int32_t num_heads, int32_t max_seq_len,
                                 float softmax_scale, void *out, float *lse, void *workspace,
                                 size_t workspace_bytes, int32_t *dev_status, void *stream) {
-  mla_status_t s = mla_decode_partial(q, cache, num_blocks, block_size, block_table,
-                                      max_blocks_per_seq, seq_lens, batch, num_heads, max_seq_len,
-                                      softmax_scale, out, lse, workspace, workspace_bytes,
-                                      dev_status, stream);
+  mla_status_t s = mla_decode_partial(q, const_cast<void *>(cache), nullptr, num_blocks,
+                                      block_size, block_table, max_blocks_per_seq, seq_lens,
+                                      batch, num_heads, max_seq_len, softmax_scale, out, lse,
+                                      workspace, workspace_bytes, dev_status, stream);
   if (s != MLA_OK || batch == 0) return s;
   return mla_combine_planned(workspace, workspace_bytes, batch, num_heads, out, lse, stream);
 }

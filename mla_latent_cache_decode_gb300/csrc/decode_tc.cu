@@ -82,7 +82,7 @@ struct __align__(1024) Smem {
   // in one phase.  No warp gets two tiles ahead (S of tile g+2 waits for the
   // P V of tile g), so two barriers suffice.
   uint64_t s_full[2], p_full[2], pv_done[2];
-  uint64_t qown_full, q_full, q_tmem, q_free, fin_qk, fin_pv;
+  uint64_t qown_full, q_full, q_tmem, q_free, fin_qk, fin_pv, row_ready;
   // upcoming tiles, per producer: block-table entries [0, 4), first token [4]
   int32_t tab[2][kTabRing][8];
   uint32_t tmem_base;
@@ -113,6 +113,8 @@ struct Params {
   void *ws;
   int32_t max_ranges;
   int32_t *dev_status;
+  const uint4 *kv_new;  // optional: row b is request b's newest token, stored before decoding
+  uint4 *cache_rows;    // the cache, for those stores
 };
 
 // Segments of range p, in plan order: request b, tokens [t0, t1), partial
@@ -199,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&s.pv_done[i]), 1);
     }
     mbar_init(smem_u32(&s.qown_full), 1);
+    mbar_init(smem_u32(&s.row_ready), 1);
     mbar_init(smem_u32(&s.q_full), 1);
     mbar_init(smem_u32(&s.q_tmem), 1);  // tcgen05.commit of the Q-own copy
     mbar_init(smem_u32(&s.q_free), 2);  // both S issuers
@@ -289,6 +292,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int slot = g % kSlots;
           const uint32_t par = ((g / kSlots) & 1u) ^ 1u;
+          // the tile holding a request's newest row, when this launch stores it
+          if (prm.kv_new && tt + kTile >= t1 && t1 == v.seq_len[it.b] &&
+              !mbar_wait(smem_u32(&s.row_ready), 0, abort_flag, kWaitBudgetNs)) {
+            set_abort(s, prm.dev_status);
+            ok = false;
+            break;
+          }
           if (own_role) {
             // the first segment's Q own dims are staged in the own ring: its
             // first loads wait until they have been copied to tensor memory
@@ -506,6 +516,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         report(prm.dev_status, MLA_ERR_DEVICE_TIMEOUT);
     }
   } else if (warp == 9) {
+    // ------------------------------------------------------------ appended rows
+    // With kv_new, request b's newest row (token seq_len[b] - 1) is stored
+    // into its slot by the CTAs whose range holds that token, before their
+    // producers load the tile holding it: the warp writes the rows, orders
+    // them before the async proxy's reads, and signals row_ready.  Both CTAs
+    // of the pair store the same bytes, each before its own loads.
+    if (active && prm.kv_new) {
+      SegIter it;
+      it.init(v, prm.batch, pair);
+      int32_t t0, t1, slot_p;
+      while (it.next(t0, t1, slot_p)) {
+        const int32_t L = v.seq_len[it.b];
+        if (t1 != L || L == 0) continue;  // not the request's last segment
+        const int32_t pos = L - 1;
+        const int32_t blk = prm.block_table[(int64_t)it.b * prm.max_blocks_per_seq + pos / BS];
+        if (blk < 0 || blk >= prm.num_blocks) {
+          if (lane == 0) report(prm.dev_status, MLA_ERR_DEVICE_RANGE);
+          continue;
+        }
+        const int64_t row = (int64_t)blk * BS + pos % BS;
+        const uint4 *src = prm.kv_new + (int64_t)it.b * (kRow / 8);
+        uint4 *dst = prm.cache_rows + row * (kRow / 8);
+        for (int k = lane; k < kRow / 8; k += 32) dst[k] = __ldg(src + k);
+      }
+      fence_proxy_async_global();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&s.row_ready));
+    }
     // ------------------------------------------------------------ Q loader
     // Q of every segment's request, once the previous segment's S MMAs are
     // done with the Q buffers: first its own 256 dims (and rope), from where
@@ -884,7 +922,8 @@ cudaError_t ensure_smem_attr(int dev, size_t smem) {
 cudaError_t launch_decode_tc(const void *q, const void *cache, int64_t num_blocks, int32_t block_size,
                              const int32_t *block_table, int32_t max_blocks_per_seq, int32_t batch,
                              float softmax_scale, void *out, float *lse, void *ws,
-                             int32_t max_ranges, int32_t *dev_status, cudaStream_t stream) {
+                             int32_t max_ranges, int32_t *dev_status, cudaStream_t stream,
+                             const void *kv_new) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -908,6 +947,8 @@ cudaError_t launch_decode_tc(const void *q, const void *cache, int64_t num_block
   p.ws = ws;
   p.max_ranges = max_ranges;
   p.dev_status = dev_status;
+  p.kv_new = (const uint4 *)kv_new;
+  p.cache_rows = (uint4 *)const_cast<void *>(cache);
   tc::decode_tc_kernel<<<2 * max_ranges, tc::kThreads, smem, stream>>>(maps, p);
   return cudaGetLastError();
 }

@@ -410,6 +410,90 @@ def test_partial_then_combine_equals_planned(mla):
     assert torch.equal(outs[0][1], outs[1][1])
 
 
+def test_fused_append_config1_against_oracle(mla):
+    """mla_decode_append_planned: the cache after it equals the oracle's append
+    with the decode step's slot mapping, and the outputs match the oracle."""
+    w = mi.workload(1)
+    for q_kind in ("normal", "sharp"):
+        d = mi.make_host_layer(w, mi.rng_for(1), q_kind=q_kind)
+        cache = dev_bf16(d["cache"])
+        q, kv = dev_bf16(d["q"]), dev_bf16(d["kv_new"])
+        bt, sl = dev(d["block_table"], torch.int32), dev(d["seq_lens"], torch.int32)
+        B = d["q"].shape[0]
+        out = torch.full((B, 128, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((B, 128), float("nan"), dtype=torch.float32, device="cuda")
+        ws = mla.make_workspace(B)
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        mla.mla_decode_plan(sl, bt, w.block_size, ws, dev_status=status)
+        mla.mla_decode_append_planned(q, cache, kv, bt, sl, d["softmax_scale"], out, lse,
+                                      workspace=ws, dev_status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        ref_cache, ref, ref_lse = oracle_layer(d)
+        assert np.array_equal(host_bits(cache), ref_cache)
+        assert_close(host_f64(out), ref, f"fused append config1 {q_kind}")
+        assert_lse_close(lse.cpu().numpy(), ref_lse)
+
+
+@pytest.mark.parametrize("workload_id", [4, 5])
+def test_fused_append_equals_separate_append(mla, workload_id):
+    """The fused path gives the same bits as mla_cache_append + mla_decode_planned
+    (split and unsplit requests, one and several segments per range)."""
+    w = mi.workload(workload_id)
+    res = []
+    for fused in (False, True):
+        dl = mi.make_device_layer(w, 0, "cuda", q_kind="sharp")
+        ws = mla.make_workspace(w.batch)
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        mla.mla_decode_plan(dl["seq_lens"], dl["block_table"], w.block_size, ws, dev_status=status)
+        out = torch.empty((w.batch, 128, 512), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((w.batch, 128), dtype=torch.float32, device="cuda")
+        args = (dl["q"], dl["cache"])
+        if fused:
+            mla.mla_decode_append_planned(dl["q"], dl["cache"], dl["kv_new"], dl["block_table"],
+                                          dl["seq_lens"], dl["softmax_scale"], out, lse,
+                                          workspace=ws, dev_status=status)
+        else:
+            mla.mla_cache_append(dl["kv_new"], dl["slot_mapping"], dl["cache"], dev_status=status)
+            mla.mla_decode_planned(dl["q"], dl["cache"], dl["block_table"], dl["seq_lens"],
+                                   dl["softmax_scale"], out, lse, workspace=ws, dev_status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        res.append((out, lse, dl["cache"].view(torch.int16).clone()))
+        del dl, args
+    assert torch.equal(res[0][2], res[1][2]), "caches differ"
+    assert torch.equal(res[0][0].view(torch.int16), res[1][0].view(torch.int16))
+    assert torch.equal(res[0][1], res[1][1])
+
+
+def test_fused_append_skips_empty_requests(mla):
+    lens = [0, 5, 0, 130, 1]
+    w = mi.custom_workload([max(L, 1) for L in lens], block_size=16, append=True, pool_factor=2)
+    d = mi.make_host_layer(w, np.random.default_rng(31))
+    d["seq_lens"] = np.array(lens, np.int32)
+    cache = dev_bf16(d["cache"])
+    B = len(lens)
+    out = torch.empty((B, 128, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, 128), dtype=torch.float32, device="cuda")
+    bt, sl = dev(d["block_table"], torch.int32), dev(d["seq_lens"], torch.int32)
+    ws = mla.make_workspace(B)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.mla_decode_plan(sl, bt, 16, ws, dev_status=status)
+    mla.mla_decode_append_planned(dev_bf16(d["q"]), cache, dev_bf16(d["kv_new"]), bt, sl,
+                                  d["softmax_scale"], out, lse, workspace=ws, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    slots = np.array([mi.slot_of(d["block_table"], b, L - 1, 16) if L > 0 else -1
+                      for b, L in enumerate(lens)], np.int64)
+    ref_cache = d["cache"].copy()
+    oracle.append(d["kv_new"], slots, ref_cache)
+    assert np.array_equal(host_bits(cache), ref_cache)
+    got = host_f64(out)
+    ro, rl = oracle.decode(d["q"], ref_cache, d["block_table"], d["seq_lens"], d["softmax_scale"])
+    assert_close(got, ro, "fused append with empty requests")
+    assert_lse_close(lse.cpu().numpy(), rl)
+
+
 def test_config5_mixed_fragmented_sampled(mla):
     w = mi.workload(5)
     bt = mi.make_block_table(mi.rng_for(5, 0, 1), w.seq_lens, w.block_size, w.num_blocks())
@@ -433,8 +517,9 @@ def test_config5_mixed_fragmented_sampled(mla):
 
 
 def test_config3_dp_rank_61_layers_sampled(mla):
-    """The benchmark's launch configuration: one plan per step, then append +
-    planned decode per layer, each layer with its own cache, shared table."""
+    """The benchmark's launch configuration: one plan per step, then per layer
+    the fused append + planned decode, each layer with its own cache, shared
+    table; sampled requests against the oracle, and the appended rows."""
     w = mi.workload(3)
     bt = mi.make_block_table(mi.rng_for(3, 0, 1), w.seq_lens, w.block_size, w.num_blocks())
     ws = mla.make_workspace(w.batch)
@@ -452,12 +537,19 @@ def test_config3_dp_rank_61_layers_sampled(mla):
                         seq_lens=dl["seq_lens"].cpu().numpy(), kv_new=mi.to_bits(dl["kv_new"]),
                         slot_mapping=dl["slot_mapping"].cpu().numpy(),
                         softmax_scale=dl["softmax_scale"])
-        out, lse = _gpu_layer(mla, dl, ws, status, planned=True)
+        out = torch.empty((w.batch, 128, 512), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((w.batch, 128), dtype=torch.float32, device="cuda")
+        mla.mla_decode_append_planned(dl["q"], dl["cache"], dl["kv_new"], dl["block_table"],
+                                      dl["seq_lens"], dl["softmax_scale"], out, lse,
+                                      workspace=ws, dev_status=status)
         if host is not None:
             torch.cuda.synchronize()
             ref, ref_lse = _oracle_sample(host, reqs)
             assert_close(host_f64(out)[reqs], ref, f"config3 layer {layer}")
             assert_lse_close(lse.cpu().numpy()[reqs], ref_lse)
+            slots = host["slot_mapping"]
+            got_rows = mi.to_bits(dl["cache"]).reshape(-1, 576)[slots]
+            assert np.array_equal(got_rows, host["kv_new"]), f"config3 layer {layer} appended rows"
         del dl
     torch.cuda.synchronize()
     assert int(status.item()) == 0
