@@ -136,7 +136,8 @@ mla_status_t mla_decode_plan(const int32_t *seq_lens, int32_t batch, int32_t num
  *   seq_lens      int32 [batch] (device) context lengths; 0 gives out = 0 and
  *                 lse = -inf for that request.
  *   max_seq_len   host upper bound of seq_lens (checked against the table).
- *   softmax_scale multiplies q . row (e.g. 1/sqrt(192) for 128 + 64 dim heads).
+ *   softmax_scale multiplies q . row (e.g. 1/sqrt(192) for 128 + 64 dim heads);
+ *                 positive and finite, else MLA_ERR_INVALID_ARGUMENT.
  *   out           bf16 [batch, num_heads, 512] (written).
  *   lse           fp32 [batch, num_heads] natural-log sum-exp, or NULL.
  *   workspace     device scratch of >= mla_decode_workspace_size(batch,

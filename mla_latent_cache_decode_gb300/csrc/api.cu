@@ -99,8 +99,8 @@ mla_status_t check_decode_args(const void *q, const void *cache, int64_t num_blo
   if (max_seq_len < 0 || (int64_t)max_seq_len > (int64_t)max_blocks_per_seq * block_size)
     return fail(MLA_ERR_INVALID_ARGUMENT, "max_seq_len %d outside [0, %lld]", max_seq_len,
                 (long long)max_blocks_per_seq * block_size);
-  if (!std::isfinite(softmax_scale))
-    return fail(MLA_ERR_INVALID_ARGUMENT, "softmax_scale is not finite");
+  if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f))
+    return fail(MLA_ERR_INVALID_ARGUMENT, "softmax_scale must be positive and finite");
   const size_t need = mla_decode_workspace_size(batch, num_heads);
   if (need == 0) return fail(MLA_ERR_CUDA, "cannot query the current device");
   if (workspace_bytes < need)

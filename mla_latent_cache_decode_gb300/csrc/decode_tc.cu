@@ -635,18 +635,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(lane_addr + buf_col + 32, &xr[32]);
           tmem_wait_ld();
           // ---- online softmax in log2 units, lazy rescale of O (eight
-          // independent partial maxima / sums keep the dependency chains short)
+          // independent partial maxima / sums keep the dependency chains short).
+          // The scale is positive (checked on the host), so the tile max is
+          // taken on the raw scores and each exponent is one fma, s*c - m;
+          // columns past the sequence end (tail tiles only) are masked.
           float x[kTile];
           float mx[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+          if (n == kTile) {
 #pragma unroll
-          for (int k = 0; k < kTile; ++k) {
-            x[k] = k < n ? __uint_as_float(xr[k]) * prm.scale_log2 : -INFINITY;
-            mx[k & 7] = fmaxf(mx[k & 7], x[k]);
+            for (int k = 0; k < kTile; ++k) {
+              x[k] = __uint_as_float(xr[k]);
+              mx[k & 7] = fmaxf(mx[k & 7], x[k]);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < kTile; ++k) {
+              x[k] = k < n ? __uint_as_float(xr[k]) : -INFINITY;
+              mx[k & 7] = fmaxf(mx[k & 7], x[k]);
+            }
           }
           const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+                             prm.scale_log2;
           const bool rescale = first || tmax > m_used + kRescaleThreshold;
           float alpha = 1.f;
           if (rescale) {
@@ -658,9 +670,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           float ps[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) ps[k] = 0.f;
+          const float c = prm.scale_log2, nm = -m_used;
 #pragma unroll
           for (int k = 0; k < kTile; k += 2) {
-            const float p0 = ex2_approx(x[k] - m_used), p1 = ex2_approx(x[k + 1] - m_used);
+            const float p0 = ex2_approx(fmaf(x[k], c, nm)), p1 = ex2_approx(fmaf(x[k + 1], c, nm));
             ps[(k >> 1) & 7] += p0 + p1;
             pk[k / 2] = pack_bf16(p0, p1);
           }

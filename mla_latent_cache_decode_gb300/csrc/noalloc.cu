@@ -95,8 +95,8 @@ extern "C" mla_status_t mla_decode_noalloc(const void *q, const void *cache, int
       (int64_t)max_blocks_per_seq * block_size > (int64_t)INT32_MAX / 2 || max_seq_len < 0 ||
       (int64_t)max_seq_len > (int64_t)max_blocks_per_seq * block_size)
     return noalloc_fail(MLA_ERR_INVALID_ARGUMENT, "bad num_blocks, table width or max_seq_len");
-  if (!(softmax_scale == softmax_scale) || softmax_scale == INFINITY || softmax_scale == -INFINITY)
-    return noalloc_fail(MLA_ERR_INVALID_ARGUMENT, "softmax_scale is not finite");
+  if (!(softmax_scale > 0.f) || softmax_scale == INFINITY)
+    return noalloc_fail(MLA_ERR_INVALID_ARGUMENT, "softmax_scale must be positive and finite");
   int err = 0;
   void *ws = scratch_address(&err);
   if (!ws) return noalloc_fail(MLA_ERR_CUDA, "cudaGetSymbolAddress of the scratch array failed");

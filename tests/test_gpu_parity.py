@@ -268,6 +268,10 @@ def test_host_validation_errors(mla):
     with pytest.raises(mla.MlaError) as e:
         mla.mla_decode(q, cache, bt, sl, float("inf"), out)
     assert e.value.status == 1
+    for bad_scale in (0.0, -0.1, float("nan")):
+        with pytest.raises(mla.MlaError) as e:
+            mla.mla_decode(q, cache, bt, sl, bad_scale, out)
+        assert e.value.status == 1
 
 
 # ----------------------------------------------------------------------------- combine
