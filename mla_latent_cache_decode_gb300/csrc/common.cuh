@@ -42,6 +42,14 @@ struct SegRec {
   int32_t b, t0, t1, slot;
 };
 
+// Split of request b, written by the planner for the combine: its partials
+// are in ranges p0..p1 (p0 == p1: not split), stored in slots
+// 2 p0 + first_odd, 2 (p0 + 1), ..., 2 p1 (every later range starts inside
+// the request, so its segment of b is that range's first).
+struct ReqSplit {
+  int32_t p0, p1, first_odd, pad;
+};
+
 struct PlanHeader {
   int32_t total_units;  // U
   int32_t num_ranges;   // P (0 when U == 0)
@@ -61,11 +69,13 @@ struct PlanHeader {
 //   int32 counters[B * 2]     split arrival counters (left at zero)
 //   int32 seg_count[P_max]    segments of range p (0 for p >= P)
 //   SegRec seg_rec[P_max][kSegCache]
+//   ReqSplit req_split[B]
 //   fp32 lse_part[2 * P_max * H]
 //   fp32 o_part[2 * P_max][512 / 4][H][4]   (one partial's heads of four
 //                                            dims are contiguous)
 struct WorkspaceLayout {
-  size_t seq_len, unit_prefix, range_first, counters, seg_count, seg_rec, lse_part, o_part, total;
+  size_t seq_len, unit_prefix, range_first, counters, seg_count, seg_rec, req_split, lse_part,
+      o_part, total;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -79,6 +89,7 @@ __host__ __device__ inline WorkspaceLayout workspace_layout(int batch, int heads
   w.counters = o;     o = align256(o + sizeof(int32_t) * 2 * (size_t)batch);
   w.seg_count = o;    o = align256(o + sizeof(int32_t) * (size_t)max_ranges);
   w.seg_rec = o;      o = align256(o + sizeof(SegRec) * kSegCache * (size_t)max_ranges);
+  w.req_split = o;    o = align256(o + sizeof(ReqSplit) * (size_t)batch);
   w.lse_part = o;     o = align256(o + sizeof(float) * 2 * (size_t)max_ranges * heads);
   w.o_part = o;       o = align256(o + sizeof(float) * 2 * (size_t)max_ranges * heads * kVDim);
   w.total = o;
@@ -93,6 +104,7 @@ struct PlanView {
   int32_t *counters;
   const int32_t *seg_count;
   const SegRec *seg_rec;
+  const ReqSplit *req_split;
   float *lse_part;
   float *o_part;
 };
@@ -108,6 +120,7 @@ __host__ __device__ inline PlanView plan_view(void *ws, int batch, int heads, in
   v.counters = (int32_t *)(b + l.counters);
   v.seg_count = (const int32_t *)(b + l.seg_count);
   v.seg_rec = (const SegRec *)(b + l.seg_rec);
+  v.req_split = (const ReqSplit *)(b + l.req_split);
   v.lse_part = (float *)(b + l.lse_part);
   v.o_part = (float *)(b + l.o_part);
   return v;

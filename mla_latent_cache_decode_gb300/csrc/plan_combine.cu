@@ -82,6 +82,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
     range_first[p] = lo;
   }
   __syncthreads();  // range_first, prefix and the clamped lengths are visible to the block
+  // every request's split, for the combine (see ReqSplit)
+  ReqSplit *req_split = const_cast<ReqSplit *>(v.req_split);
+  for (int b = tid; b < batch; b += kPlanThreads) {
+    const int32_t Ub = prefix[b], n = prefix[b + 1] - Ub;
+    ReqSplit r;
+    r.p0 = n > 0 ? range_of(Ub, U, P) : 0;
+    r.p1 = n > 0 ? range_of(Ub + n - 1, U, P) : 0;
+    r.first_odd = n > 0 && range_begin(r.p0, U, P) < Ub ? 1 : 0;
+    r.pad = 0;
+    req_split[b] = r;
+  }
   // the first kSegCache segments of every range (see SegRec)
   int32_t *seg_count = const_cast<int32_t *>(v.seg_count);
   SegRec *seg_rec = const_cast<SegRec *>(v.seg_rec);
@@ -198,8 +209,9 @@ __device__ __forceinline__ void combine_row(const float *__restrict__ o_part,
 // them as [slot][512 / 4][128][4], so in the block of (request, 16-dim block)
 // thread h = head reads four dims of its head per load (a warp's loads are
 // 512 contiguous bytes) and accumulates its 16 dims in registers; splits are
-// taken four at a time with all their loads issued before any is used, since
-// the kernel is latency-bound.  The bf16 results are transposed through
+// taken four at a time with all their loads (log-sum-exps and data) issued
+// before any is used, since the kernel is latency-bound, and the split's
+// slots come from the plan's per-request record without any division.  The bf16 results are transposed through
 // shared memory into the [B][H][512] output (32 bytes of a row per head).
 // grid = (batch, 512 / 16), 128 threads.
 constexpr int kCombDims = 16;
@@ -211,27 +223,36 @@ __global__ void __launch_bounds__(kHeads) plan_combine_kernel(void *ws, int32_t 
                                                               float *__restrict__ lse) {
   PlanView v = plan_view(ws, batch, kHeads, max_ranges);
   const int b = blockIdx.x, d0 = blockIdx.y * kCombDims, h = threadIdx.x;
-  const int32_t U = v.hdr->total_units, P = v.hdr->num_ranges;
-  const int32_t Ub = v.unit_prefix[b], n = v.unit_prefix[b + 1] - Ub;
-  if (n == 0) return;
-  const int32_t p0 = range_of(Ub, U, P), p1 = range_of(Ub + n - 1, U, P);
-  if (p0 == p1) return;
-  const int nsplit = p1 - p0 + 1;
-  __shared__ int32_t s_slot[kHeads];
+  const ReqSplit rs = v.req_split[b];
+  if (rs.p0 == rs.p1) return;  // not split (or empty): the decode wrote it
+  const int nsplit = rs.p1 - rs.p0 + 1;
+  auto slot_of_split = [&](int k) -> int64_t {
+    return k == 0 ? 2 * rs.p0 + rs.first_odd : 2 * (rs.p0 + k);
+  };
   __shared__ __align__(16) __nv_bfloat16 tile[kHeads][kCombDims + 8];  // +8: stagger the rows
   float4 acc[kCombDims / 4];
 #pragma unroll
   for (int j = 0; j < kCombDims / 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
   float m = -INFINITY, z = 0.f;
-  // splits kHeads at a time (a request spans at most P <= max_ranges ranges);
-  // the running max rescales what was summed so far when a later chunk raises it
-  for (int base = 0; base < nsplit; base += kHeads) {
-    const int cnt = min(kHeads, nsplit - base);
-    __syncthreads();
-    if (h < cnt) s_slot[h] = partial_slot(p0 + base + h, U, P, Ub);
-    __syncthreads();
+  // splits kCombGroup at a time, all their loads issued before any is used (the
+  // kernel is latency-bound); the running max rescales what was summed so far
+  for (int k0 = 0; k0 < nsplit; k0 += kCombGroup) {
+    float l[kCombGroup];
+#pragma unroll
+    for (int u = 0; u < kCombGroup; ++u)
+      l[u] = k0 + u < nsplit ? v.lse_part[slot_of_split(k0 + u) * kHeads + h] : -INFINITY;
+    float4 x[kCombGroup][kCombDims / 4];
+#pragma unroll
+    for (int u = 0; u < kCombGroup; ++u) {
+      const int64_t w = slot_of_split(k0 + u < nsplit ? k0 + u : k0);
+      const float4 *src = reinterpret_cast<const float4 *>(v.o_part) +
+                          (w * (kVDim / 4) + d0 / 4) * kHeads + h;
+#pragma unroll
+      for (int j = 0; j < kCombDims / 4; ++j) x[u][j] = __ldg(src + (int64_t)j * kHeads);
+    }
     float mc = m;
-    for (int k = 0; k < cnt; ++k) mc = fmaxf(mc, v.lse_part[(int64_t)s_slot[k] * kHeads + h]);
+#pragma unroll
+    for (int u = 0; u < kCombGroup; ++u) mc = fmaxf(mc, l[u]);
     if (mc == -INFINITY) continue;
     if (m != -INFINITY && mc != m) {
       const float r = __expf(m - mc);
@@ -242,28 +263,14 @@ __global__ void __launch_bounds__(kHeads) plan_combine_kernel(void *ws, int32_t 
       }
     }
     m = mc;
-    for (int k0 = 0; k0 < cnt; k0 += kCombGroup) {
-      float a[kCombGroup];
-      float4 x[kCombGroup][kCombDims / 4];
 #pragma unroll
-      for (int u = 0; u < kCombGroup; ++u) {
-        const bool live = k0 + u < cnt;
-        const int64_t w = s_slot[live ? k0 + u : k0];
-        const float l = v.lse_part[w * kHeads + h];
-        a[u] = (!live || l == -INFINITY) ? 0.f : __expf(l - m);
-        const float4 *src = reinterpret_cast<const float4 *>(v.o_part) +
-                            (w * (kVDim / 4) + d0 / 4) * kHeads + h;
+    for (int u = 0; u < kCombGroup; ++u) {
+      const float a = l[u] == -INFINITY ? 0.f : __expf(l[u] - m);
+      z += a;
 #pragma unroll
-        for (int j = 0; j < kCombDims / 4; ++j) x[u][j] = __ldg(src + (int64_t)j * kHeads);
-      }
-#pragma unroll
-      for (int u = 0; u < kCombGroup; ++u) {
-        z += a[u];
-#pragma unroll
-        for (int j = 0; j < kCombDims / 4; ++j) {
-          acc[j].x += a[u] * x[u][j].x; acc[j].y += a[u] * x[u][j].y;
-          acc[j].z += a[u] * x[u][j].z; acc[j].w += a[u] * x[u][j].w;
-        }
+      for (int j = 0; j < kCombDims / 4; ++j) {
+        acc[j].x += a * x[u][j].x; acc[j].y += a * x[u][j].y;
+        acc[j].z += a * x[u][j].z; acc[j].w += a * x[u][j].w;
       }
     }
   }
@@ -276,11 +283,13 @@ __global__ void __launch_bounds__(kHeads) plan_combine_kernel(void *ws, int32_t 
         __floats2bfloat162_rn(acc[j].z * inv, acc[j].w * inv);
   }
   __syncthreads();
-  // 128 rows x 32 bytes: two 16-byte pieces per row, thread t takes pieces t + 128 k
+  // 128 rows x (2 kCombDims) bytes: kCombDims / 8 pieces of 16 bytes per row,
+  // thread t takes pieces t + 128 k
+  constexpr int kPieces = kCombDims / 8;
   __nv_bfloat16 *orow = out + (int64_t)b * kHeads * kVDim + d0;
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int piece = h + kHeads * k, row = piece >> 1, part = piece & 1;
+  for (int k = 0; k < kPieces; ++k) {
+    const int piece = h + kHeads * k, row = piece / kPieces, part = piece % kPieces;
     *reinterpret_cast<uint4 *>(orow + (int64_t)row * kVDim + part * 8) =
         *reinterpret_cast<const uint4 *>(&tile[row][part * 8]);
   }
