@@ -212,7 +212,8 @@ def run_mine(args, w, rank, world, local_rank):
     scale = mi.SOFTMAX_SCALE
 
     def step(timing_events=None):
-        mla.mla_decode_plan(W["seq"], W["bt"], w.block_size, ws, dev_status=status, stream=sh)
+        mla.mla_decode_plan(W["seq"], W["bt"], w.block_size, ws, dev_status=status, stream=sh,
+                            num_blocks=w.num_blocks())
         for l in range(L):
             d = W["layers"][l]
             # mla_decode_append_planned (the append of this step's row fused
@@ -295,7 +296,8 @@ def run_mine(args, w, rank, world, local_rank):
     def e2e_step():
         seqd.copy_(seq_host, non_blocking=True)
         btd.copy_(bt_host, non_blocking=True)
-        mla.mla_decode_plan(seqd, btd, w.block_size, ws, dev_status=status, stream=sh)
+        mla.mla_decode_plan(seqd, btd, w.block_size, ws, dev_status=status, stream=sh,
+                            num_blocks=w.num_blocks())
         for l in range(L):
             d = W["layers"][l]
             qd[l].copy_(q_host[l], non_blocking=True)

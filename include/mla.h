@@ -57,7 +57,7 @@
 extern "C" {
 #endif
 
-#define MLA_ABI_VERSION 1
+#define MLA_ABI_VERSION 2
 #define MLA_ROW_DIM 576       /* 512 kv_c + 64 k_rope per cached token */
 #define MLA_KV_LORA_RANK 512  /* value / output width */
 #define MLA_ROPE_DIM 64
@@ -111,17 +111,21 @@ size_t mla_decode_workspace_size(int32_t batch, int32_t num_heads);
 
 /*
  * mla_decode_plan — compute the split-KV plan for these sequence lengths
- * into the workspace (one small kernel).  The plan depends only on seq_lens,
- * batch, max_blocks_per_seq and block_size, so a caller decoding many layers
- * of one step with the same lengths plans once and then calls
+ * into the workspace (one small kernel).  The plan depends on seq_lens,
+ * batch, max_blocks_per_seq, block_size and — when block_table is given
+ * (device int32 [batch, max_blocks_per_seq], nullable) — on the table too: it
+ * then records where each worker's first tile lies in the cache (num_blocks
+ * is the pool size, > 0), so the decode starts loading without a table
+ * lookup; re-plan when any of them changes.  A caller decoding many layers
+ * of one step with the same lengths and table plans once and then calls
  * mla_decode_planned per layer.  Lengths are read on the device; a length
  * outside [0, max_blocks_per_seq * block_size] is clamped and reported as
  * MLA_ERR_DEVICE_RANGE.
  */
-mla_status_t mla_decode_plan(const int32_t *seq_lens, int32_t batch, int32_t num_heads,
-                             int32_t max_blocks_per_seq, int32_t block_size,
-                             void *workspace, size_t workspace_bytes, int32_t *dev_status,
-                             void *stream);
+mla_status_t mla_decode_plan(const int32_t *seq_lens, const int32_t *block_table, int32_t batch,
+                             int32_t num_heads, int32_t max_blocks_per_seq, int32_t block_size,
+                             int64_t num_blocks, void *workspace, size_t workspace_bytes,
+                             int32_t *dev_status, void *stream);
 
 /*
  * mla_decode — absorbed-form MLA decode (the equation at the top of this file).
@@ -159,8 +163,8 @@ mla_status_t mla_decode(const void *q, const void *cache, int64_t num_blocks, in
 
 /*
  * mla_decode_planned — mla_decode using the plan already in `workspace`
- * (from mla_decode_plan with the same seq_lens, batch, block_size and
- * max_blocks_per_seq).  Same arguments and results as mla_decode.
+ * (from mla_decode_plan with the same seq_lens, batch, block_size,
+ * max_blocks_per_seq and, if it was given one, block table).  Same arguments and results as mla_decode.
  */
 mla_status_t mla_decode_planned(const void *q, const void *cache, int64_t num_blocks,
                                 int32_t block_size, const int32_t *block_table,

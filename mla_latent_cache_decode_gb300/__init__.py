@@ -56,7 +56,7 @@ def _load():
     lib.mla_cache_append.restype = ctypes.c_int
     lib.mla_decode_workspace_size.argtypes = [i32, i32]
     lib.mla_decode_workspace_size.restype = sz
-    lib.mla_decode_plan.argtypes = [P, i32, i32, i32, i32, P, sz, P, P]
+    lib.mla_decode_plan.argtypes = [P, P, i32, i32, i32, i32, i64, P, sz, P, P]
     lib.mla_decode_plan.restype = ctypes.c_int
     dec = [P, P, i64, i32, P, i32, P, i32, i32, i32, f32, P, P, P, sz, P, P]
     lib.mla_decode.argtypes = dec
@@ -155,14 +155,19 @@ def mla_cache_append(kv_new, slot_mapping, cache, dev_status=None, stream=None):
 
 
 def mla_decode_plan(seq_lens, block_table, block_size, workspace, num_heads=NUM_HEADS,
-                    dev_status=None, stream=None):
+                    dev_status=None, stream=None, num_blocks=None):
+    """Split-KV plan for these lengths.  With num_blocks (the cache pool's block
+    count) the plan also records where every worker's first tile lies in the
+    cache (the plan then depends on block_table too: re-plan when it changes)."""
     import torch
     _need(seq_lens, torch.int32, 1, "seq_lens")
     _need(block_table, torch.int32, 2, "block_table")
-    _check(get_lib().mla_decode_plan(_ptr(seq_lens), seq_lens.shape[0], num_heads,
-                               block_table.shape[1], block_size, _ptr(workspace),
-                               workspace.numel() * workspace.element_size(), _ptr(dev_status),
-                               _stream(stream)))
+    table = _ptr(block_table) if num_blocks else None
+    _check(get_lib().mla_decode_plan(_ptr(seq_lens), table, seq_lens.shape[0], num_heads,
+                                     block_table.shape[1], block_size, int(num_blocks or 0),
+                                     _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(),
+                                     _ptr(dev_status), _stream(stream)))
 
 
 def _decode(fn, q, cache, block_table, seq_lens, softmax_scale, out, lse, workspace,

@@ -13,9 +13,10 @@ namespace mla {
 cudaError_t launch_cache_append(const void *kv_new, const int64_t *slots, int64_t num_tokens,
                                 void *cache, int64_t num_slots, int32_t *dev_status,
                                 cudaStream_t stream);
-cudaError_t launch_plan(const int32_t *seq_lens, int32_t batch, int32_t unit_tokens,
-                        int32_t max_blocks_per_seq, int32_t block_size, int32_t max_ranges,
-                        void *ws, int32_t heads, int32_t *dev_status, cudaStream_t stream);
+cudaError_t launch_plan(const int32_t *seq_lens, const int32_t *block_table, int64_t num_blocks,
+                        int32_t batch, int32_t unit_tokens, int32_t max_blocks_per_seq,
+                        int32_t block_size, int32_t max_ranges, void *ws, int32_t heads,
+                        int32_t *dev_status, cudaStream_t stream);
 cudaError_t launch_plan_combine(void *ws, int32_t batch, int32_t heads, int32_t max_ranges,
                                 void *out, float *lse, cudaStream_t stream);
 cudaError_t launch_offsets_combine(const float *o_part, const float *lse_part,
@@ -161,9 +162,10 @@ size_t mla_decode_workspace_size(int32_t batch, int32_t num_heads) {
   return workspace_layout(batch, num_heads, ranges).total;
 }
 
-mla_status_t mla_decode_plan(const int32_t *seq_lens, int32_t batch, int32_t num_heads,
-                             int32_t max_blocks_per_seq, int32_t block_size, void *workspace,
-                             size_t workspace_bytes, int32_t *dev_status, void *stream) {
+mla_status_t mla_decode_plan(const int32_t *seq_lens, const int32_t *block_table, int32_t batch,
+                             int32_t num_heads, int32_t max_blocks_per_seq, int32_t block_size,
+                             int64_t num_blocks, void *workspace, size_t workspace_bytes,
+                             int32_t *dev_status, void *stream) {
   g_detail.clear();
   if (batch < 0) return fail(MLA_ERR_INVALID_ARGUMENT, "batch < 0");
   if (num_heads != kHeads) return fail(MLA_ERR_UNSUPPORTED, "num_heads must be %d", kHeads);
@@ -176,9 +178,11 @@ mla_status_t mla_decode_plan(const int32_t *seq_lens, int32_t batch, int32_t num
   if (need == 0) return fail(MLA_ERR_CUDA, "cannot query the current device");
   if (workspace_bytes < need)
     return fail(MLA_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu", workspace_bytes, need);
-  cudaError_t e = launch_plan(seq_lens, batch, tc_unit_tokens(), max_blocks_per_seq,
-                              block_size, max_ranges_current(), workspace, num_heads, dev_status,
-                              (cudaStream_t)stream);
+  if (block_table && num_blocks <= 0)
+    return fail(MLA_ERR_INVALID_ARGUMENT, "num_blocks must be > 0 with a block table");
+  cudaError_t e = launch_plan(seq_lens, block_table, num_blocks, batch, tc_unit_tokens(),
+                              max_blocks_per_seq, block_size, max_ranges_current(), workspace,
+                              num_heads, dev_status, (cudaStream_t)stream);
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "plan launch");
 }
 
@@ -264,8 +268,8 @@ mla_status_t mla_decode(const void *q, const void *cache, int64_t num_blocks, in
                                      max_blocks_per_seq, seq_lens, batch, num_heads, max_seq_len,
                                      softmax_scale, out, lse, workspace, workspace_bytes);
   if (s != MLA_OK || batch == 0) return s;
-  s = mla_decode_plan(seq_lens, batch, num_heads, max_blocks_per_seq, block_size, workspace,
-                      workspace_bytes, dev_status, stream);
+  s = mla_decode_plan(seq_lens, block_table, batch, num_heads, max_blocks_per_seq, block_size,
+                      num_blocks, workspace, workspace_bytes, dev_status, stream);
   if (s != MLA_OK) return s;
   return mla_decode_planned(q, cache, num_blocks, block_size, block_table, max_blocks_per_seq,
                             seq_lens, batch, num_heads, max_seq_len, softmax_scale, out, lse,

@@ -35,11 +35,15 @@ __device__ __forceinline__ void report(int32_t *dev_status, int32_t code) {
 // ---------------------------------------------------------------------------
 // The first kSegCache segments of every range, written by the planner so that
 // a worker learns its work with one memory round trip: request b, tokens
-// [t0, t1), and the partial slot (-1: the request is not split, the segment
-// writes the output directly).  Later segments are found by walking the plan.
+// [t0, t1), the partial slot (-1: the request is not split, the segment
+// writes the output directly), and — when the plan was given the block table
+// and pages hold at least a tile — the cache row of the segment's first token
+// (row0, -1 if unknown), so its first tile can be loaded without a table
+// lookup.  Later segments are found by walking the plan.
 constexpr int kSegCache = 4;
-struct SegRec {
+struct __align__(16) SegRec {
   int32_t b, t0, t1, slot;
+  int32_t row0, pad0, pad1, pad2;
 };
 
 // Split of request b, written by the planner for the combine: its partials

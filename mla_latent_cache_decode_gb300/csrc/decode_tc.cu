@@ -124,25 +124,31 @@ struct Params {
 struct SegIter {
   PlanView v;
   int32_t batch, p, n, idx, b;
+  int32_t row0;  // cache row of the current segment's first token, -1 if unknown
+  SegRec first;  // record 0, loaded together with the count
   __device__ void init(const PlanView &pv, int32_t batch_, int32_t p_) {
     v = pv;
     batch = batch_;
     p = p_;
     n = v.seg_count[p];
+    first = v.seg_rec[(int64_t)p * kSegCache];  // independent of n: one round trip for both
     idx = 0;
     b = -1;
+    row0 = -1;
   }
   __device__ bool next(int32_t &t0, int32_t &t1, int32_t &slot) {
     if (idx >= n) return false;
     if (idx < kSegCache) {
-      const SegRec r = v.seg_rec[(int64_t)p * kSegCache + idx];
+      const SegRec r = idx == 0 ? first : v.seg_rec[(int64_t)p * kSegCache + idx];
       ++idx;
       b = r.b;
       t0 = r.t0;
       t1 = r.t1;
       slot = r.slot;
+      row0 = r.row0;
       return true;
     }
+    row0 = -1;
     const int32_t U = v.hdr->total_units, P = v.hdr->num_ranges;
     const int32_t r0 = range_begin(p, U, P), r1 = range_begin(p + 1, U, P);
     for (++b; b < batch; ++b) {
@@ -274,21 +280,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (ok && it.next(t0, t1, slot_p)) {
         for (int32_t tt = t0; tt < t1; tt += kTile, ++g) {
           fetch_next();
-          // this tile's entries (and those of the tile kOtherAhead later) have landed
-          cp_async_wait<kTabAhead - kOtherAhead>();
-          // cache rows of the tile's boxes (one box per page, or one per tile)
+          // cache rows of the tile's boxes (one box per page, or one per tile):
+          // a segment's first tile from the plan's record when it has one,
+          // else from the fetched block-table entries
           const int nbx = (min(kTile, t1 - tt) + box_rows - 1) / box_rows;
-          const int32_t *e = tab + (g % kTabRing) * 8;
           int32_t y[kTile / 16];
+          if (tt == t0 && it.row0 >= 0 && big_pages) {
+            y[0] = it.row0;
+          } else {
+            // this tile's entries (and those of the tile kOtherAhead later) have landed
+            cp_async_wait<kTabAhead - kOtherAhead>();
+            const int32_t *e = tab + (g % kTabRing) * 8;
 #pragma unroll
-          for (int j = 0; j < kTile / 16; ++j) {
-            if (j >= nbx) break;
-            int32_t blk = e[j];
-            if (blk < 0 || blk >= nb) {
-              if (own_role) report(prm.dev_status, MLA_ERR_DEVICE_RANGE);
-              blk = 0;
+            for (int j = 0; j < kTile / 16; ++j) {
+              if (j >= nbx) break;
+              int32_t blk = e[j];
+              if (blk < 0 || blk >= nb) {
+                if (own_role) report(prm.dev_status, MLA_ERR_DEVICE_RANGE);
+                blk = 0;
+              }
+              y[j] = blk * BS + ((tt + j * box_rows) % BS);
             }
-            y[j] = blk * BS + ((tt + j * box_rows) % BS);
           }
           const int slot = g % kSlots;
           const uint32_t par = ((g / kSlots) & 1u) ^ 1u;

@@ -7,9 +7,10 @@
 #include "common.cuh"
 
 namespace mla {
-cudaError_t launch_plan(const int32_t *seq_lens, int32_t batch, int32_t unit_tokens,
-                        int32_t max_blocks_per_seq, int32_t block_size, int32_t max_ranges,
-                        void *ws, int32_t heads, int32_t *dev_status, cudaStream_t stream);
+cudaError_t launch_plan(const int32_t *seq_lens, const int32_t *block_table, int64_t num_blocks,
+                        int32_t batch, int32_t unit_tokens, int32_t max_blocks_per_seq,
+                        int32_t block_size, int32_t max_ranges, void *ws, int32_t heads,
+                        int32_t *dev_status, cudaStream_t stream);
 cudaError_t launch_plan_combine(void *ws, int32_t batch, int32_t heads, int32_t max_ranges,
                                 void *out, float *lse, cudaStream_t stream);
 int tc_unit_tokens();
@@ -101,8 +102,9 @@ extern "C" mla_status_t mla_decode_noalloc(const void *q, const void *cache, int
   void *ws = scratch_address(&err);
   if (!ws) return noalloc_fail(MLA_ERR_CUDA, "cudaGetSymbolAddress of the scratch array failed");
   cudaStream_t st = (cudaStream_t)stream;
-  cudaError_t e = launch_plan(seq_lens, batch, tc_unit_tokens(), max_blocks_per_seq, block_size,
-                              ranges, ws, num_heads, dev_status, st);
+  cudaError_t e = launch_plan(seq_lens, block_table, num_blocks, batch, tc_unit_tokens(),
+                              max_blocks_per_seq, block_size, ranges, ws, num_heads, dev_status,
+                              st);
   if (e == cudaSuccess)
     e = launch_decode_tc(q, cache, num_blocks, block_size, block_table, max_blocks_per_seq, batch,
                          softmax_scale, out, lse, ws, ranges, dev_status, st);

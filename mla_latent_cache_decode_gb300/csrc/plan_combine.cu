@@ -13,6 +13,8 @@ namespace mla {
 constexpr int kPlanThreads = 1024;
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__restrict__ seq_lens,
+                                                            const int32_t *__restrict__ block_table,
+                                                            int64_t num_blocks,
                                                             int32_t batch, int32_t unit_tokens,
                                                             int32_t max_blocks_per_seq,
                                                             int32_t block_size, int32_t max_ranges,
@@ -110,6 +112,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
           r.t0 = (u0 - Ub) * unit_tokens;
           r.t1 = min((u1 - Ub) * unit_tokens, seq_out[b]);
           r.slot = range_of(Ub, U, P) != range_of(Ue - 1, U, P) ? partial_slot(p, U, P, Ub) : -1;
+          r.row0 = -1;
+          if (block_table && block_size >= unit_tokens && r.t0 < r.t1) {
+            const int32_t blk =
+                block_table[(int64_t)b * max_blocks_per_seq + r.t0 / block_size];
+            if (blk >= 0 && (int64_t)blk < num_blocks) r.row0 = blk * block_size + r.t0 % block_size;
+          }
+          r.pad0 = r.pad1 = r.pad2 = 0;
           seg_rec[(int64_t)p * kSegCache + n] = r;
         }
         ++n;
@@ -130,11 +139,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
   }
 }
 
-cudaError_t launch_plan(const int32_t *seq_lens, int32_t batch, int32_t unit_tokens,
-                        int32_t max_blocks_per_seq, int32_t block_size, int32_t max_ranges,
-                        void *ws, int32_t heads, int32_t *dev_status, cudaStream_t stream) {
-  plan_kernel<<<1, kPlanThreads, 0, stream>>>(seq_lens, batch, unit_tokens, max_blocks_per_seq,
-                                              block_size, max_ranges, ws, heads, dev_status);
+cudaError_t launch_plan(const int32_t *seq_lens, const int32_t *block_table, int64_t num_blocks,
+                        int32_t batch, int32_t unit_tokens, int32_t max_blocks_per_seq,
+                        int32_t block_size, int32_t max_ranges, void *ws, int32_t heads,
+                        int32_t *dev_status, cudaStream_t stream) {
+  plan_kernel<<<1, kPlanThreads, 0, stream>>>(seq_lens, block_table, num_blocks, batch,
+                                              unit_tokens, max_blocks_per_seq, block_size,
+                                              max_ranges, ws, heads, dev_status);
   return cudaGetLastError();
 }
 

@@ -41,7 +41,7 @@ def test_binding_names_match_header():
 def test_status_strings_and_version(lib):
     lib.mla_status_string.restype = ctypes.c_char_p
     lib.mla_abi_version.restype = ctypes.c_int
-    assert lib.mla_abi_version() == 1
+    assert lib.mla_abi_version() == 2
     names = [lib.mla_status_string(i).decode() for i in range(7)]
     assert names[0] == "MLA_OK" and names[6] == "MLA_ERR_DEVICE_TIMEOUT"
     assert lib.mla_status_string(99).decode() == "MLA_ERR_UNKNOWN"

@@ -509,7 +509,8 @@ def test_config5_mixed_fragmented_sampled(mla):
         dl, host = _device_layer_and_host(w, layer, block_table=bt)
         if layer == 0:
             seq = dl["seq_lens"]
-            mla.mla_decode_plan(seq, dl["block_table"], w.block_size, ws, dev_status=status)
+            mla.mla_decode_plan(seq, dl["block_table"], w.block_size, ws, dev_status=status,
+                                num_blocks=w.num_blocks())
         out, lse = _gpu_layer(mla, dl, ws, status, planned=True)
         torch.cuda.synchronize()
         assert int(status.item()) == 0
@@ -534,7 +535,7 @@ def test_config3_dp_rank_61_layers_sampled(mla):
         dl = mi.make_device_layer(w, layer, "cuda", block_table=bt)
         if layer == 0:
             mla.mla_decode_plan(dl["seq_lens"], dl["block_table"], w.block_size, ws,
-                                dev_status=status)
+                                dev_status=status, num_blocks=w.num_blocks())
         host = None
         if layer in sample_layers:
             host = dict(q=mi.to_bits(dl["q"]), cache=mi.to_bits(dl["cache"]), block_table=bt,
