@@ -63,10 +63,6 @@ constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;  // S buffers at kColS +
 constexpr uint64_t kWaitBudgetNs = 100000000ull;  // 100 ms per wait, far above any legal wait
 constexpr uint64_t kDrainBudgetNs = 10000000ull;  // 10 ms to drain in-flight copies on abort
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
-constexpr int kTabAhead = 4;                      // tiles the block-table entries are fetched ahead
-constexpr int kTabRing = 8;                       // ring of fetched entries (> kTabAhead)
-constexpr int kOtherAhead = 2;                    // other part prefetched into L2 this many tiles
-                                                  // ahead (0: off; < kTabAhead)
 
 struct __align__(1024) Smem {
   uint8_t q_other[4][kQChunkBytes];      // Q[:, other 256 dims], 4 chunks of 64 dims: 64 KB
@@ -83,14 +79,19 @@ struct __align__(1024) Smem {
   // P V of tile g), so two barriers suffice.
   uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t qown_full, q_full, q_tmem, q_free, fin_qk, fin_pv, row_ready;
-  // upcoming tiles, per producer: block-table entries [0, 4), first token [4]
-  int32_t tab[2][kTabRing][8];
+  uint64_t stage_free;  // one phase: the staged first Q own dims have been copied
   uint32_t tmem_base;
   int abort;
 };
 
-static_assert(sizeof(((Smem *)0)->own) == 4 * kQChunkBytes,
-              "the first segment's Q own dims are staged in the own ring");
+// At launch the first segment's Q own dims (four 16 KB chunks) are staged in
+// slot 1 of both rings, which stay empty until tile 1: chunks 0-1 in the
+// other ring's slot 1, chunks 2-3 in the own ring's slot 1.  Tile 0's loads
+// then need not wait for the copy into tensor memory.
+__device__ __forceinline__ uint8_t *q_stage_chunk(Smem &s, int c) {
+  return c < 2 ? s.other[1][2 * c] : s.own[1][2 * (c - 2)];
+}
+static_assert(2 * kChunkBytes == kQChunkBytes, "a Q chunk is two cache chunks");
 
 // Tensor maps over the cache viewed as [rows = NB*BS][576]: 3-D views
 // {64 columns, rows, 9 chunks} (chunk stride 128 B) fetch several 64-dim
@@ -208,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_u32(&s.qown_full), 1);
     mbar_init(smem_u32(&s.row_ready), 1);
+    mbar_init(smem_u32(&s.stage_free), 1);
     mbar_init(smem_u32(&s.q_full), 1);
     mbar_init(smem_u32(&s.q_tmem), 1);  // tcgen05.commit of the Q-own copy
     mbar_init(smem_u32(&s.q_free), 2);  // both S issuers
@@ -246,30 +248,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int box_rows = BS < kTile ? BS : kTile;
       const uint32_t box_bytes = (uint32_t)(box_rows * 128);
       const int64_t nb = prm.num_blocks;
-      // Block-table entries of upcoming tiles are fetched kTabAhead tiles
-      // ahead by cp.async into a small ring: a plain load here would stall
-      // this thread for a memory latency on every tile before its copy could
-      // be issued.
-      int32_t *tab = &s.tab[own_role ? 0 : 1][0][0];
+      // Block-table entries of the next tile are loaded one tile ahead into
+      // registers: plain loads whose latency overlaps this tile's slot wait.
+      // A segment's first tile needs none when the plan's record has its row.
       SegIter fc;
       fc.init(v, prm.batch, pair);
       int32_t fc_t = 0, fc_t1 = 0, fc_slot;
       bool fc_more = true;
-      uint32_t fc_g = 0;
-      auto fetch_next = [&]() {  // entries of the next tile (if any), as one group
-        while (fc_more && fc_t >= fc_t1) fc_more = fc.next(fc_t, fc_t1, fc_slot);
-        if (fc_more) {
+      int32_t nxt[kTile / 16];
+      auto load_next = [&]() {  // move the cursor one tile on and load that tile's entries
+        bool first = false;
+        while (fc_more && fc_t >= fc_t1) {
+          fc_more = fc.next(fc_t, fc_t1, fc_slot);
+          first = true;
+        }
+        if (!fc_more) return;
+        if (!(first && fc.row0 >= 0 && big_pages)) {
           const int32_t *row = prm.block_table + (int64_t)fc.b * prm.max_blocks_per_seq;
           const int nbx = (min(kTile, fc_t1 - fc_t) + box_rows - 1) / box_rows;
-          int32_t *dst = tab + (fc_g % kTabRing) * 8;
-          for (int j = 0; j < nbx; ++j) cp_async_4(smem_u32(dst + j), row + (fc_t + j * box_rows) / BS);
-          dst[4] = fc_t;
-          fc_t += kTile;
-          ++fc_g;
+#pragma unroll
+          for (int j = 0; j < kTile / 16; ++j)
+            if (j < nbx) nxt[j] = row[(fc_t + j * box_rows) / BS];
         }
-        cp_async_commit();
+        fc_t += kTile;
       };
-      for (int i = 0; i < kTabAhead; ++i) fetch_next();
+      load_next();
       if (own_role) {
         prefetch_tmap(&maps.kv4);
       } else {
@@ -279,22 +282,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       while (ok && it.next(t0, t1, slot_p)) {
         for (int32_t tt = t0; tt < t1; tt += kTile, ++g) {
-          fetch_next();
           // cache rows of the tile's boxes (one box per page, or one per tile):
           // a segment's first tile from the plan's record when it has one,
-          // else from the fetched block-table entries
+          // else from the entries loaded one tile ago
           const int nbx = (min(kTile, t1 - tt) + box_rows - 1) / box_rows;
           int32_t y[kTile / 16];
           if (tt == t0 && it.row0 >= 0 && big_pages) {
             y[0] = it.row0;
           } else {
-            // this tile's entries (and those of the tile kOtherAhead later) have landed
-            cp_async_wait<kTabAhead - kOtherAhead>();
-            const int32_t *e = tab + (g % kTabRing) * 8;
 #pragma unroll
             for (int j = 0; j < kTile / 16; ++j) {
               if (j >= nbx) break;
-              int32_t blk = e[j];
+              int32_t blk = nxt[j];
               if (blk < 0 || blk >= nb) {
                 if (own_role) report(prm.dev_status, MLA_ERR_DEVICE_RANGE);
                 blk = 0;
@@ -302,6 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               y[j] = blk * BS + ((tt + j * box_rows) % BS);
             }
           }
+          load_next();  // the next tile's entries, consumed one iteration later
           const int slot = g % kSlots;
           const uint32_t par = ((g / kSlots) & 1u) ^ 1u;
           // the tile holding a request's newest row, when this launch stores it
@@ -312,9 +312,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           if (own_role) {
-            // the first segment's Q own dims are staged in the own ring: its
-            // first loads wait until they have been copied to tensor memory
-            if (g == 0 && !mbar_wait(smem_u32(&s.q_tmem), 0, abort_flag, kWaitBudgetNs)) {
+            // slot 1 stages the first segment's Q own dims until they have
+            // been copied to tensor memory
+            if (g == 1 && !mbar_wait(smem_u32(&s.stage_free), 0, abort_flag, kWaitBudgetNs)) {
               set_abort(s, prm.dev_status);
               ok = false;
               break;
@@ -338,6 +338,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           } else {
+            if (g == 1 && !mbar_wait(smem_u32(&s.stage_free), 0, abort_flag, kWaitBudgetNs)) {
+              set_abort(s, prm.dev_status);
+              ok = false;
+              break;
+            }
             if (!mbar_wait(smem_u32(&s.other_empty[slot]), par, abort_flag, kWaitBudgetNs)) {
               set_abort(s, prm.dev_status);
               ok = false;
@@ -361,26 +366,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    c < 4 ? 64 * (oth0 + c) : 512, y[j], bar, policy);
               }
             }
-            if (kOtherAhead > 0 && big_pages && g + kOtherAhead < fc_g) {
-              // L2 prefetch of the other part of the tile kOtherAhead later
-              // (its entries are in the ring; a slot is refilled only when it
-              // frees, too late to hide an HBM read)
-              const int32_t *e2 = tab + ((g + kOtherAhead) % kTabRing) * 8;
-              int32_t blk = e2[0];
-              if (blk >= 0 && blk < nb) {
-                const int32_t y2 = blk * BS + (e2[4] % BS);
-                if (half == 0) {
-                  tma_prefetch_3d(&maps.kv5, 0, y2, 4);
-                } else {
-                  tma_prefetch_3d(&maps.kv4, 0, y2, 0);
-                  tma_prefetch_3d(&maps.kv1, 0, y2, 8);
-                }
-              }
-            }
           }
         }
       }
-      cp_async_wait<0>();  // no copy into the ring outlives the thread
       if (s.abort) {
         // the consumers gave up: let the last issued loads land before exit
         for (int i = 0; i < kSlots; ++i)
@@ -409,7 +397,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t d_own = smem_desc(smem_u32(s.own[0][0]), 16, 1024, kSwizzle128B);
       const uint64_t d_oth = smem_desc(smem_u32(s.other[0][0]), 16, 1024, kSwizzle128B);
       const uint64_t d_q = smem_desc(smem_u32(s.q_other[0]), 16, 1024, kSwizzle128B);
-      const uint64_t d_qstart = smem_desc(smem_u32(s.own[0][0]), 16, 1024, kSwizzle128B);
       const uint64_t d_rope = smem_desc(smem_u32(s.q_rope), 16, 1024, kSwizzle128B);
       const uint32_t a_q = tmem + kColQ;
       bool ok = true;
@@ -420,17 +407,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (par == 0) {
           // Q[:, own 256 dims] into tensor memory: 16 copies of 128 rows x 16
-          // dims, addressed like the A operand.  Staged in the (still empty)
-          // own ring for the first segment, in the Q buffers afterwards.
-          const uint64_t d_src = seg == 0 ? d_qstart : d_q;
+          // dims, addressed like the A operand.  Staged in the rings' slot 1
+          // for the first segment, in the Q buffers afterwards.
           tc_fence_after();
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 4; ++c) {
+            const uint64_t d_src =
+                seg == 0 ? smem_desc(smem_u32(q_stage_chunk(s, c)), 16, 1024, kSwizzle128B)
+                         : d_q + (uint64_t)((c * kQChunkBytes) >> 4);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              tmem_cp_128x256b(a_q + c * 32 + kk * 8,
-                               d_src + (uint64_t)((c * kQChunkBytes + kk * 32) >> 4));
+              tmem_cp_128x256b(a_q + c * 32 + kk * 8, d_src + (uint64_t)((kk * 32) >> 4));
+          }
           mma_commit(smem_u32(&s.q_tmem));
+          if (seg == 0) mma_commit(smem_u32(&s.stage_free));
         }
         if (!mbar_wait(smem_u32(&s.q_tmem), seg & 1u, abort_flag, kWaitBudgetNs) ||
             !mbar_wait(smem_u32(&s.q_full), seg & 1u, abort_flag, kWaitBudgetNs)) {
@@ -573,13 +563,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           set_abort(s, prm.dev_status);
           break;
         }
-        // own dims: into the own ring for the first segment (empty until the
-        // copy is done, so Q's other dims need not wait), else the Q buffers
-        uint8_t *own_stage = seg == 0 ? s.own[0][0] : s.q_other[0];
+        // own dims: into the rings' slot 1 for the first segment (empty until
+        // the copy is done, so Q's other dims need not wait), else the Q buffers
         mbar_arrive_expect_tx(smem_u32(&s.qown_full), 5 * kQChunkBytes);
         for (int c = 0; c < 4; ++c)
-          tma_load_2d(smem_u32(own_stage + c * kQChunkBytes), &maps.q, 64 * (own0 + c),
-                      it.b * kHeads, smem_u32(&s.qown_full));
+          tma_load_2d(smem_u32(seg == 0 ? q_stage_chunk(s, c) : s.q_other[c]), &maps.q,
+                      64 * (own0 + c), it.b * kHeads, smem_u32(&s.qown_full));
         tma_load_2d(smem_u32(s.q_rope), &maps.q, 512, it.b * kHeads, smem_u32(&s.qown_full));
         {  // the next segment's Q rows into L2 meanwhile
           SegIter nx = it;
