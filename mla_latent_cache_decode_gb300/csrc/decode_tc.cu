@@ -251,8 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Block-table entries of the next tile are loaded one tile ahead into
       // registers: plain loads whose latency overlaps this tile's slot wait.
       // A segment's first tile needs none when the plan's record has its row.
-      SegIter fc;
-      fc.init(v, prm.batch, pair);
+      SegIter fc = it;  // shares the first record load
       int32_t fc_t = 0, fc_t1 = 0, fc_slot;
       bool fc_more = true;
       int32_t nxt[kTile / 16];
