@@ -150,7 +150,9 @@ mla_status_t mla_decode_plan(const int32_t *seq_lens, const int32_t *block_table
  *                 reads).  Calls sharing one workspace must not overlap on
  *                 the GPU.
  * Requirements: num_heads == 128; block_size in {16, 32, 64, 128, 256};
- * max_seq_len <= max_blocks_per_seq * block_size; batch >= 0 (0 = no-op).
+ * max_seq_len <= max_blocks_per_seq * block_size <= 2^30; batch *
+ * ceil(max_blocks_per_seq * block_size / 64) < 2^31 (the plan counts 64-token
+ * units in int32); batch >= 0 (0 = no-op).  Else MLA_ERR_INVALID_ARGUMENT.
  * Rows the plan does not cover (tails past seq_len, unused blocks) are never
  * read, whatever they hold.
  */

@@ -95,8 +95,8 @@ mla_status_t check_decode_args(const void *q, const void *cache, int64_t num_blo
     return fail(MLA_ERR_INVALID_ARGUMENT, "num_blocks %lld out of range", (long long)num_blocks);
   if (max_blocks_per_seq <= 0)
     return fail(MLA_ERR_INVALID_ARGUMENT, "max_blocks_per_seq %d <= 0", max_blocks_per_seq);
-  if ((int64_t)max_blocks_per_seq * block_size > (int64_t)INT32_MAX / 2)
-    return fail(MLA_ERR_INVALID_ARGUMENT, "max_blocks_per_seq * block_size too large");
+  if (!plan_fits(batch, max_blocks_per_seq, block_size, tc_unit_tokens()))
+    return fail(MLA_ERR_INVALID_ARGUMENT, "batch * max_blocks_per_seq * block_size too large");
   if (max_seq_len < 0 || (int64_t)max_seq_len > (int64_t)max_blocks_per_seq * block_size)
     return fail(MLA_ERR_INVALID_ARGUMENT, "max_seq_len %d outside [0, %lld]", max_seq_len,
                 (long long)max_blocks_per_seq * block_size);
@@ -174,6 +174,8 @@ mla_status_t mla_decode_plan(const int32_t *seq_lens, const int32_t *block_table
   if (!seq_lens || !workspace) return fail(MLA_ERR_INVALID_ARGUMENT, "null pointer");
   if (!aligned(workspace, 256)) return fail(MLA_ERR_INVALID_ARGUMENT, "workspace alignment");
   if (max_blocks_per_seq <= 0) return fail(MLA_ERR_INVALID_ARGUMENT, "max_blocks_per_seq <= 0");
+  if (!plan_fits(batch, max_blocks_per_seq, block_size, tc_unit_tokens()))
+    return fail(MLA_ERR_INVALID_ARGUMENT, "batch * max_blocks_per_seq * block_size too large");
   const size_t need = mla_decode_workspace_size(batch, num_heads);
   if (need == 0) return fail(MLA_ERR_CUDA, "cannot query the current device");
   if (workspace_bytes < need)

@@ -24,15 +24,41 @@ __device__ __forceinline__ void report(int32_t *dev_status, int32_t code) {
 //
 // Every request b is cut into units of kUnit tokens; unit u of the flattened
 // sequence (requests in order) is U_b + i for the i-th unit of request b.
-// The U units are split into P contiguous ranges, range p = [R_p, R_{p+1}),
-// R_p = floor(p * U / P), P = min(P_max, U).  Range p is processed by one
-// worker (a CTA pair for the tensor-core kernel).  A request whose units lie
-// in one range is written directly; a request spanning k ranges leaves k
-// fp32 partials which are merged by log-sum-exp.  Range p holds at most two
-// partial segments (its first and its last), stored in slots 2p and 2p+1:
-// the segment of request b in range p uses slot 2p if R_p >= U_b (the range
-// starts inside or at b) and 2p+1 otherwise.
+// The U units are split into P = min(P_max, U) contiguous, non-empty ranges,
+// range p = [R_p, R_{p+1}), R_0 = 0, R_P = U, stored in range_start.  Range p
+// is processed by one worker (a CTA pair for the tensor-core kernel).  The
+// boundaries balance cost rather than units: a range costs kUnitCost per unit
+// plus kSegmentCost for every request that starts inside it, since each
+// segment after a worker's first stages a new query, writes the previous
+// segment's result and refills the pipeline.  R_p is the unit at cost
+// p * C / P along the batch (C the total cost, each request's start cost
+// placed before its units; a target inside a start cost snaps to the
+// request's first unit), then moved the least needed to keep every range
+// non-empty.  A request whose units lie in one range is written directly; a
+// request spanning k ranges leaves k fp32 partials which are merged by
+// log-sum-exp.  Range p holds at most two partial segments (its first and its
+// last), stored in slots 2p and 2p+1: the segment of request b in range p
+// uses slot 2p if R_p >= U_b (the range starts inside or at b) and 2p+1
+// otherwise.
 // ---------------------------------------------------------------------------
+constexpr int64_t kUnitCost = 2;
+constexpr int64_t kSegmentCost = 7;  // 3.5 units: a segment switch, measured
+
+// Units are counted in int32: the longest batch the table allows must fit.
+inline bool plan_fits(int32_t batch, int32_t max_blocks_per_seq, int32_t block_size,
+                      int32_t unit_tokens) {
+  const int64_t max_len = (int64_t)max_blocks_per_seq * block_size;
+  return max_len <= (int64_t)INT32_MAX / 2 &&
+         (int64_t)batch * ((max_len + unit_tokens - 1) / unit_tokens) <= (int64_t)INT32_MAX;
+}
+
+// Partial slot of the segment of request b (units [Ub, Ue)) in range p =
+// [r0, r1), -1 when the request lies wholly in the range.
+__host__ __device__ inline int32_t segment_slot(int32_t p, int32_t r0, int32_t r1, int32_t Ub,
+                                                int32_t Ue) {
+  return Ub < r0 || Ue > r1 ? 2 * p + (r0 < Ub ? 1 : 0) : -1;
+}
+
 // The first kSegCache segments of every range, written by the planner so that
 // a worker learns its work with one memory round trip: request b, tokens
 // [t0, t1), the partial slot (-1: the request is not split, the segment
@@ -69,7 +95,9 @@ struct PlanHeader {
 //   PlanHeader
 //   int32 seq_len[B]          clamped lengths
 //   int32 unit_prefix[B + 1]  U_b
+//   int32 range_start[P_max + 1]  R_p (entries past P hold U)
 //   int32 range_first[P_max]  first request with units in range p
+//   int64 cost_prefix[B + 1]  cost before request b (planner scratch)
 //   int32 counters[B * 2]     split arrival counters (left at zero)
 //   int32 seg_count[P_max]    segments of range p (0 for p >= P)
 //   SegRec seg_rec[P_max][kSegCache]
@@ -78,7 +106,7 @@ struct PlanHeader {
 //   fp32 o_part[2 * P_max][512 / 4][H][4]   (one partial's heads of four
 //                                            dims are contiguous)
 struct WorkspaceLayout {
-  size_t seq_len, unit_prefix, range_first, counters, seg_count, seg_rec, req_split, lse_part,
+  size_t seq_len, unit_prefix, range_start, range_first, cost_prefix, counters, seg_count, seg_rec, req_split, lse_part,
       o_part, total;
 };
 
@@ -89,7 +117,9 @@ __host__ __device__ inline WorkspaceLayout workspace_layout(int batch, int heads
   size_t o = align256(sizeof(PlanHeader));
   w.seq_len = o;      o = align256(o + sizeof(int32_t) * (size_t)batch);
   w.unit_prefix = o;  o = align256(o + sizeof(int32_t) * ((size_t)batch + 1));
+  w.range_start = o;  o = align256(o + sizeof(int32_t) * ((size_t)max_ranges + 1));
   w.range_first = o;  o = align256(o + sizeof(int32_t) * ((size_t)max_ranges + 1));
+  w.cost_prefix = o;  o = align256(o + sizeof(int64_t) * ((size_t)batch + 1));
   w.counters = o;     o = align256(o + sizeof(int32_t) * 2 * (size_t)batch);
   w.seg_count = o;    o = align256(o + sizeof(int32_t) * (size_t)max_ranges);
   w.seg_rec = o;      o = align256(o + sizeof(SegRec) * kSegCache * (size_t)max_ranges);
@@ -104,7 +134,9 @@ struct PlanView {
   const PlanHeader *hdr;
   const int32_t *seq_len;
   const int32_t *unit_prefix;
+  const int32_t *range_start;
   const int32_t *range_first;
+  const int64_t *cost_prefix;
   int32_t *counters;
   const int32_t *seg_count;
   const SegRec *seg_rec;
@@ -120,7 +152,9 @@ __host__ __device__ inline PlanView plan_view(void *ws, int batch, int heads, in
   v.hdr = (const PlanHeader *)b;
   v.seq_len = (const int32_t *)(b + l.seq_len);
   v.unit_prefix = (const int32_t *)(b + l.unit_prefix);
+  v.range_start = (const int32_t *)(b + l.range_start);
   v.range_first = (const int32_t *)(b + l.range_first);
+  v.cost_prefix = (const int64_t *)(b + l.cost_prefix);
   v.counters = (int32_t *)(b + l.counters);
   v.seg_count = (const int32_t *)(b + l.seg_count);
   v.seg_rec = (const SegRec *)(b + l.seg_rec);
@@ -128,19 +162,6 @@ __host__ __device__ inline PlanView plan_view(void *ws, int batch, int heads, in
   v.lse_part = (float *)(b + l.lse_part);
   v.o_part = (float *)(b + l.o_part);
   return v;
-}
-
-__host__ __device__ inline int32_t range_begin(int32_t p, int32_t U, int32_t P) {
-  return (int32_t)(((int64_t)p * U) / P);
-}
-
-// Range holding unit u (0 <= u < U): the largest p with R_p <= u.
-__host__ __device__ inline int32_t range_of(int32_t u, int32_t U, int32_t P) {
-  return (int32_t)((((int64_t)u + 1) * P - 1) / U);
-}
-
-__host__ __device__ inline int32_t partial_slot(int32_t p, int32_t U, int32_t P, int32_t Ub) {
-  return 2 * p + (range_begin(p, U, P) < Ub ? 1 : 0);
 }
 
 }  // namespace mla

@@ -150,8 +150,7 @@ struct SegIter {
       return true;
     }
     row0 = -1;
-    const int32_t U = v.hdr->total_units, P = v.hdr->num_ranges;
-    const int32_t r0 = range_begin(p, U, P), r1 = range_begin(p + 1, U, P);
+    const int32_t r0 = v.range_start[p], r1 = v.range_start[p + 1];
     for (++b; b < batch; ++b) {
       const int32_t Ub = v.unit_prefix[b];
       if (Ub >= r1) return false;
@@ -160,7 +159,7 @@ struct SegIter {
       if (u0 >= u1) continue;
       t0 = (u0 - Ub) * kTile;
       t1 = min((u1 - Ub) * kTile, v.seq_len[b]);
-      slot = range_of(Ub, U, P) != range_of(Ue - 1, U, P) ? partial_slot(p, U, P, Ub) : -1;
+      slot = segment_slot(p, r0, r1, Ub, Ue);
       ++idx;
       return true;
     }

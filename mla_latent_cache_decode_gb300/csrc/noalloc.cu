@@ -93,7 +93,7 @@ extern "C" mla_status_t mla_decode_noalloc(const void *q, const void *cache, int
       block_size != 256)
     return noalloc_fail(MLA_ERR_UNSUPPORTED, "block_size not in {16,32,64,128,256}");
   if (num_blocks <= 0 || num_blocks > (int64_t)INT32_MAX || max_blocks_per_seq <= 0 ||
-      (int64_t)max_blocks_per_seq * block_size > (int64_t)INT32_MAX / 2 || max_seq_len < 0 ||
+      !plan_fits(batch, max_blocks_per_seq, block_size, tc_unit_tokens()) || max_seq_len < 0 ||
       (int64_t)max_seq_len > (int64_t)max_blocks_per_seq * block_size)
     return noalloc_fail(MLA_ERR_INVALID_ARGUMENT, "bad num_blocks, table width or max_seq_len");
   if (!(softmax_scale > 0.f) || softmax_scale == INFINITY)

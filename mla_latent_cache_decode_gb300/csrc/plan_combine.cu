@@ -11,6 +11,7 @@
 namespace mla {
 
 constexpr int kPlanThreads = 1024;
+constexpr int kMaxPlanRanges = 1024;  // boundaries are settled in shared memory
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__restrict__ seq_lens,
                                                             const int32_t *__restrict__ block_table,
@@ -23,17 +24,22 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
   PlanView v = plan_view(ws, batch, heads, max_ranges);
   int32_t *seq_out = const_cast<int32_t *>(v.seq_len);
   int32_t *prefix = const_cast<int32_t *>(v.unit_prefix);
+  int32_t *range_start = const_cast<int32_t *>(v.range_start);
   int32_t *range_first = const_cast<int32_t *>(v.range_first);
-  __shared__ int32_t warp_sums[kPlanThreads / 32];
-  __shared__ int32_t carry;
+  int64_t *cost_prefix = const_cast<int64_t *>(v.cost_prefix);
+  __shared__ int64_t warp_sums[kPlanThreads / 32];
+  __shared__ int64_t carry;
+  __shared__ int32_t bound[kMaxPlanRanges + 1];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int64_t max_len = (int64_t)max_blocks_per_seq * block_size;
   if (tid == 0) carry = 0;
   __syncthreads();
-  // exclusive scan of units per request, in chunks of kPlanThreads
+  // Exclusive scan of (non-empty requests, units) per request, packed in one
+  // int64 (count in the high word, units in the low; the host bounds the
+  // total units below 2^31, so the low word never carries).
   for (int base = 0; base < batch; base += kPlanThreads) {
     const int b = base + tid;
-    int32_t units = 0;
+    int64_t item = 0;
     if (b < batch) {
       int32_t L = seq_lens[b];
       if (L < 0 || (int64_t)L > max_len) {
@@ -41,41 +47,106 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
         L = L < 0 ? 0 : (int32_t)max_len;
       }
       seq_out[b] = L;
-      units = (L + unit_tokens - 1) / unit_tokens;
+      const int32_t units = (L + unit_tokens - 1) / unit_tokens;
+      item = units > 0 ? (int64_t(1) << 32) | units : 0;
       v.counters[2 * b] = 0;
       v.counters[2 * b + 1] = 0;
     }
-    int32_t x = units;
+    int64_t x = item;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+      const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
       if (lane >= o) x += y;
     }
     if (lane == 31) warp_sums[wid] = x;
     __syncthreads();
     if (wid == 0) {
-      int32_t s = warp_sums[lane];
+      int64_t s = warp_sums[lane];
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        int32_t y = __shfl_up_sync(0xffffffffu, s, o);
+        const int64_t y = __shfl_up_sync(0xffffffffu, s, o);
         if (lane >= o) s += y;
       }
       warp_sums[lane] = s;  // inclusive over warps
     }
     __syncthreads();
-    const int32_t incl = x + (wid > 0 ? warp_sums[wid - 1] : 0) + carry;
-    if (b < batch) prefix[b] = incl - units;
+    const int64_t incl = x + (wid > 0 ? warp_sums[wid - 1] : 0) + carry;
+    if (b < batch) {
+      const int64_t excl = incl - item;
+      prefix[b] = (int32_t)(excl & 0xffffffff);
+      cost_prefix[b] = kUnitCost * (excl & 0xffffffff) + kSegmentCost * (excl >> 32);
+    }
     __syncthreads();
     if (tid == kPlanThreads - 1) carry = incl;
     __syncthreads();
   }
-  const int32_t U = carry;
-  if (tid == 0) prefix[batch] = U;
+  const int32_t U = (int32_t)(carry & 0xffffffff);
+  const int64_t C = kUnitCost * U + kSegmentCost * (carry >> 32);
+  if (tid == 0) {
+    prefix[batch] = U;
+    cost_prefix[batch] = C;
+  }
   const int32_t P = U < max_ranges ? U : max_ranges;
+  // Range boundaries.  First the unit at cost p*C/P, held as R_p - p ...
+  for (int p = tid; p <= P; p += kPlanThreads) {
+    int32_t r = 0;
+    if (p == P) {
+      r = U;
+    } else if (p > 0) {
+      const int64_t c = (int64_t)p * C / P;
+      int lo = 0, hi = batch - 1;  // the request whose cost span holds c
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cost_prefix[mid] <= c) lo = mid; else hi = mid - 1;
+      }
+      const int64_t x = c - cost_prefix[lo];
+      const int64_t k = x < kSegmentCost ? 0 : (x - kSegmentCost + kUnitCost / 2) / kUnitCost;
+      const int32_t n = prefix[lo + 1] - prefix[lo];
+      r = prefix[lo] + (int32_t)(k < n ? k : n);
+    }
+    bound[p] = r - p;
+  }
   __syncthreads();
+  // ... then the least change that makes them strictly increasing with
+  // R_0 = 0 and R_P = U: R_p = p + min over q >= p of (max over q' <= q of
+  // (R_q' - q')), the last term pinned to U - P.  One warp, 32 at a time.
+  if (wid == 0 && P > 0) {
+    int32_t run = INT32_MIN;
+    for (int base = 0; base <= P; base += 32) {
+      const int p = base + lane;
+      int32_t x = p <= P ? bound[p] : INT32_MIN;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x = max(x, y);
+      }
+      x = max(x, run);
+      if (p <= P) bound[p] = x;
+      run = __shfl_sync(0xffffffffu, x, 31);
+    }
+    __syncwarp();
+    if (lane == 0) bound[P] = U - P;
+    __syncwarp();
+    run = INT32_MAX;
+    for (int top = P; top >= 0; top -= 32) {
+      const int p = top - lane;
+      int32_t x = p >= 0 ? bound[p] : INT32_MAX;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x = min(x, y);
+      }
+      x = min(x, run);
+      run = __shfl_sync(0xffffffffu, x, 31);
+      __syncwarp();
+      if (p >= 0) bound[p] = x + p;
+    }
+  }
+  __syncthreads();
+  for (int p = tid; p <= max_ranges; p += kPlanThreads) range_start[p] = p <= P ? bound[p] : U;
   // first request of every range: the largest b with prefix[b] <= R_p
   for (int p = tid; p < P; p += kPlanThreads) {
-    const int32_t r = range_begin(p, U, P);
+    const int32_t r = bound[p];
     int lo = 0, hi = batch - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -85,13 +156,21 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
   }
   __syncthreads();  // range_first, prefix and the clamped lengths are visible to the block
   // every request's split, for the combine (see ReqSplit)
+  auto range_of = [&](int32_t u) {  // the largest p < P with R_p <= u
+    int lo = 0, hi = P - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (bound[mid] <= u) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+  };
   ReqSplit *req_split = const_cast<ReqSplit *>(v.req_split);
   for (int b = tid; b < batch; b += kPlanThreads) {
     const int32_t Ub = prefix[b], n = prefix[b + 1] - Ub;
     ReqSplit r;
-    r.p0 = n > 0 ? range_of(Ub, U, P) : 0;
-    r.p1 = n > 0 ? range_of(Ub + n - 1, U, P) : 0;
-    r.first_odd = n > 0 && range_begin(r.p0, U, P) < Ub ? 1 : 0;
+    r.p0 = n > 0 ? range_of(Ub) : 0;
+    r.p1 = n > 0 ? range_of(Ub + n - 1) : 0;
+    r.first_odd = n > 0 && bound[r.p0] < Ub ? 1 : 0;
     r.pad = 0;
     req_split[b] = r;
   }
@@ -101,7 +180,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
   for (int p = tid; p < max_ranges; p += kPlanThreads) {
     int32_t n = 0;
     if (p < P) {
-      const int32_t r0 = range_begin(p, U, P), r1 = range_begin(p + 1, U, P);
+      const int32_t r0 = bound[p], r1 = bound[p + 1];
       for (int b = range_first[p]; b < batch && prefix[b] < r1; ++b) {
         const int32_t Ub = prefix[b], Ue = prefix[b + 1];
         const int32_t u0 = max(r0, Ub), u1 = min(r1, Ue);
@@ -111,7 +190,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
           r.b = b;
           r.t0 = (u0 - Ub) * unit_tokens;
           r.t1 = min((u1 - Ub) * unit_tokens, seq_out[b]);
-          r.slot = range_of(Ub, U, P) != range_of(Ue - 1, U, P) ? partial_slot(p, U, P, Ub) : -1;
+          r.slot = segment_slot(p, r0, r1, Ub, Ue);
           r.row0 = -1;
           if (block_table && block_size >= unit_tokens && r.t0 < r.t1) {
             const int32_t blk =
@@ -143,6 +222,9 @@ cudaError_t launch_plan(const int32_t *seq_lens, const int32_t *block_table, int
                         int32_t batch, int32_t unit_tokens, int32_t max_blocks_per_seq,
                         int32_t block_size, int32_t max_ranges, void *ws, int32_t heads,
                         int32_t *dev_status, cudaStream_t stream) {
+  if (max_ranges < 1 || max_ranges > kMaxPlanRanges ||
+      !plan_fits(batch, max_blocks_per_seq, block_size, unit_tokens))
+    return cudaErrorInvalidValue;
   plan_kernel<<<1, kPlanThreads, 0, stream>>>(seq_lens, block_table, num_blocks, batch,
                                               unit_tokens, max_blocks_per_seq, block_size,
                                               max_ranges, ws, heads, dev_status);
