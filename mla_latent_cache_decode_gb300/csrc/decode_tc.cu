@@ -78,6 +78,10 @@ struct __align__(1024) Smem {
   // in one phase.  No warp gets two tiles ahead (S of tile g+2 waits for the
   // P V of tile g), so two barriers suffice.
   uint64_t s_full[2], p_full[2], pv_done[2];
+  // P V of that buffer's tile issued: the tensor pipe runs MMAs in issue
+  // order, so the next S MMAs into the buffer may be issued behind it (the
+  // fences around the barrier order the two issuers' MMAs).
+  uint64_t pv_issued[2];
   uint64_t qown_full, q_full, q_tmem, q_free, fin_qk, fin_pv, row_ready;
   uint64_t stage_free;  // one phase: the staged first Q own dims have been copied
   uint32_t tmem_base;
@@ -205,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&s.s_full[i]), 1);
       mbar_init(smem_u32(&s.p_full[i]), kSoftmaxThreads);
       mbar_init(smem_u32(&s.pv_done[i]), 1);
+      mbar_init(smem_u32(&s.pv_issued[i]), 1);
     }
     mbar_init(smem_u32(&s.qown_full), 1);
     mbar_init(smem_u32(&s.row_ready), 1);
@@ -432,10 +437,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int slot = g % kSlots;
           const uint32_t ph = (g / kSlots) & 1u;
           const uint32_t d_s = tmem + kColS + 64 * (g & 1u);
-          // the S buffer is free once P V of tile g-2 (which read P from it) is done
+          // the S buffer may be overwritten behind P V of tile g-2 (which reads
+          // P from it): that P V must have been issued
           if (!mbar_wait(smem_u32(&s.other_full[slot]), ph, abort_flag, kWaitBudgetNs) ||
-              (g >= 2 && !mbar_wait(smem_u32(&s.pv_done[g & 1u]), ((g >> 1) - 1) & 1u, abort_flag,
-                                    kWaitBudgetNs))) {
+              (g >= 2 && !mbar_wait(smem_u32(&s.pv_issued[g & 1u]), ((g >> 1) - 1) & 1u,
+                                    abort_flag, kWaitBudgetNs))) {
             set_abort(s, prm.dev_status);
             ok = false;
             break;
@@ -507,6 +513,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kt = 0; kt < ksteps; ++kt)
             mma_ts(tmem + kColO, a_p + kt * 8, bw + (uint64_t)((kt * 2048) >> 4), id_pv,
                    (tt > t0 || kt > 0) ? 1u : 0u);
+          tc_fence_before();
+          mbar_arrive(smem_u32(&s.pv_issued[g & 1u]));
           mma_commit(smem_u32(&s.pv_done[g & 1u]));
           mma_commit(smem_u32(&s.own_empty[slot]));
         }
