@@ -355,6 +355,10 @@ def run_mine(args, w, rank, world, local_rank):
                    "cuda_graph": graph is not None,
                    "parallelism": "dp-attention rank per GPU; replicas only"},
         "step_roofline_frac": round(roofline_step_us / (ms_step * 1e3), 4),
+        # all algorithmic bytes of the step (cache rows + q + out + appended
+        # rows) per second, and against the nominal ~8 TB/s of GB300's HBM3e
+        "algorithmic_gbs": round(world * step_bytes / (ms_step * 1e-3) / 1e9, 2),
+        "step_frac_of_nominal_8tbs": round(step_bytes / (ms_step * 1e-3) / 8e12, 4),
         "roofline": {"bound": "hbm", "kernel": "decode_tc_kernel (mla_decode_partial)",
                      "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "peak_source": src,
