@@ -82,6 +82,10 @@ struct __align__(1024) Smem {
   // order, so the next S MMAs into the buffer may be issued behind it (the
   // fences around the barrier order the two issuers' MMAs).
   uint64_t pv_issued[2];
+  // S MMAs of tile g all issued: the two S issuers take turns tile by tile, so
+  // the pipe finishes one tile's S before the next (its softmax, P V and the
+  // S-buffer reuse two tiles on depend on it) instead of interleaving both.
+  uint64_t qk_seq[2];
   uint64_t qown_full, q_full, q_tmem, q_free, fin_qk, fin_pv, row_ready;
   uint64_t stage_free;  // one phase: the staged first Q own dims have been copied
   uint32_t tmem_base;
@@ -210,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&s.p_full[i]), kSoftmaxThreads);
       mbar_init(smem_u32(&s.pv_done[i]), 1);
       mbar_init(smem_u32(&s.pv_issued[i]), 1);
+      mbar_init(smem_u32(&s.qk_seq[i]), 1);
     }
     mbar_init(smem_u32(&s.qown_full), 1);
     mbar_init(smem_u32(&s.row_ready), 1);
@@ -383,6 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ S = Q K^T issuers
     // Warp 1 issues the S MMAs of even tiles, warp 8 those of odd tiles: one
     // thread cannot issue N = 64 MMAs as fast as the tensor pipe runs them.
+    // They take turns (qk_seq), one whole tile each.
     // Tile g uses S buffer g & 1 and ring slot g % 2, so the two never touch
     // the same accumulator or operands.  Both wait for every segment's Q and
     // both release it (q_free counts two arrivals); the even issuer also
@@ -437,6 +443,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int slot = g % kSlots;
           const uint32_t ph = (g / kSlots) & 1u;
           const uint32_t d_s = tmem + kColS + 64 * (g & 1u);
+          if (g >= 1 && !mbar_wait(smem_u32(&s.qk_seq[(g - 1) & 1u]), ((g - 1) >> 1) & 1u,
+                                   abort_flag, kWaitBudgetNs)) {
+            set_abort(s, prm.dev_status);
+            ok = false;
+            break;
+          }
           // the S buffer may be overwritten behind P V of tile g-2 (which reads
           // P from it): that P V must have been issued
           if (!mbar_wait(smem_u32(&s.other_full[slot]), ph, abort_flag, kWaitBudgetNs) ||
@@ -479,6 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          bw + (uint64_t)((c * kChunkBytes + kk * 32) >> 4), id);
           }
           mma_commit(smem_u32(&s.s_full[g & 1u]));
+          mbar_arrive(smem_u32(&s.qk_seq[g & 1u]));
         }
         if (!ok) break;
         mma_commit(smem_u32(&s.q_free));  // Q of this segment no longer read
