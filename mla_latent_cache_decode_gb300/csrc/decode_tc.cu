@@ -135,12 +135,15 @@ struct SegIter {
   int32_t batch, p, n, idx, b;
   int32_t row0;  // cache row of the current segment's first token, -1 if unknown
   SegRec first;  // record 0, loaded together with the count
-  __device__ void init(const PlanView &pv, int32_t batch_, int32_t p_) {
+  // n_ and first_: the range's segment count and first record, loaded by the
+  // caller at kernel entry (one round trip for both, overlapping the setup)
+  __device__ void init(const PlanView &pv, int32_t batch_, int32_t p_, int32_t n_,
+                       const SegRec &first_) {
     v = pv;
     batch = batch_;
     p = p_;
-    n = v.seg_count[p];
-    first = v.seg_rec[(int64_t)p * kSegCache];  // independent of n: one round trip for both
+    n = n_;
+    first = first_;
     idx = 0;
     b = -1;
     row0 = -1;
@@ -201,6 +204,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int pair = blockIdx.x >> 1;
   const PlanView v = plan_view(prm.ws, prm.batch, kHeads, prm.max_ranges);
   const volatile int *abort_flag = &s.abort;
+  // this range's segment count and first segment record, requested before the
+  // setup below so that their latency overlaps it
+  const int32_t seg_n = v.seg_count[pair];
+  const SegRec seg_first = v.seg_rec[(int64_t)pair * kSegCache];
 
   if (tid == 0) {
     for (int i = 0; i < kSlots; ++i) {
@@ -236,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
 
-  const bool active = v.seg_count[pair] > 0;  // ranges past the plan's count have none
+  const bool active = seg_n > 0;  // ranges past the plan's count have none
   const int own0 = half * 4;        // first own 64-dim chunk (of the 8 kv_c chunks)
   const int oth0 = (1 - half) * 4;  // first other chunk
   const int BS = prm.block_size;
@@ -251,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // extra DRAM reads on a 64 x 4096 layer)
       const uint64_t policy = policy_evict_normal();
       SegIter it;
-      it.init(v, prm.batch, pair);
+      it.init(v, prm.batch, pair, seg_n, seg_first);
       int32_t t0, t1, slot_p;
       uint32_t g = 0;
       const int box_rows = BS < kTile ? BS : kTile;
@@ -396,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t par = warp == 8 ? 1u : 0u;
     if (active && elect_one_sync()) {
       SegIter it;
-      it.init(v, prm.batch, pair);
+      it.init(v, prm.batch, pair, seg_n, seg_first);
       int32_t t0, t1, slot_p;
       uint32_t g = 0, seg = 0;
       const uint32_t id = idesc_bf16_f32(128, kTile, 0);
@@ -504,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ O += P V issuer
     if (active && elect_one_sync()) {
       SegIter it;
-      it.init(v, prm.batch, pair);
+      it.init(v, prm.batch, pair, seg_n, seg_first);
       int32_t t0, t1, slot_p;
       uint32_t g = 0;
       const uint32_t id_pv = idesc_bf16_f32(128, kVHalf, 1);
@@ -545,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // of the pair store the same bytes, each before its own loads.
     if (active && prm.kv_new) {
       SegIter it;
-      it.init(v, prm.batch, pair);
+      it.init(v, prm.batch, pair, seg_n, seg_first);
       int32_t t0, t1, slot_p;
       while (it.next(t0, t1, slot_p)) {
         const int32_t L = v.seq_len[it.b];
@@ -573,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tile loads never wait behind Q.
     if (active && elect_one_sync()) {
       SegIter it;
-      it.init(v, prm.batch, pair);
+      it.init(v, prm.batch, pair, seg_n, seg_first);
       int32_t t0, t1, slot_p;
       uint32_t seg = 0;
       prefetch_tmap(&maps.q);
@@ -628,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (active) {
       SegIter it;
-      it.init(v, prm.batch, pair);
+      it.init(v, prm.batch, pair, seg_n, seg_first);
       int32_t t0, t1, slot_p;
       uint32_t g = 0;  // tiles so far
       bool ok = true;
