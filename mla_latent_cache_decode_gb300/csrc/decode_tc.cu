@@ -36,10 +36,10 @@
 //
 // Warp roles: warp 0 loads the own parts; warp 3 loads the other parts;
 // warp 9 loads every segment's Q; warps 1 and 8 issue
-// the S MMAs of even and odd tiles (warp 1 owns the tensor memory
-// allocation); warp 2 issues the P V MMAs;
+// the S MMAs of even and odd tiles; warp 2 issues the P V MMAs;
 // warps 4-7 (one thread per head) run the online softmax with lazy rescaling
-// of O and write the output (or split partials plus log-sum-exp).
+// of O and write the output (or split partials plus log-sum-exp); warp 4 owns
+// the tensor memory allocation.
 #include <atomic>
 #include <mutex>
 
@@ -88,6 +88,9 @@ struct __align__(1024) Smem {
   uint64_t qk_seq[2];
   uint64_t qown_full, q_full, q_tmem, q_free, fin_qk, fin_pv, row_ready;
   uint64_t stage_free;  // one phase: the staged first Q own dims have been copied
+  // one phase: every warp is done with its role (all its tensor-memory work,
+  // the operations it issued complete)
+  uint64_t roles_done;
   uint32_t tmem_base;
   int abort;
 };
@@ -231,13 +234,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&s.q_free), 2);  // both S issuers
     mbar_init(smem_u32(&s.fin_qk), 2);
     mbar_init(smem_u32(&s.fin_pv), 1);
+    mbar_init(smem_u32(&s.roles_done), kThreads / 32);
     s.abort = 0;
     fence_mbarrier_init_cluster();
   }
-  if (warp == 1) {
+  if (warp == 4) {  // a softmax warp: among the last to finish, it also frees it
     tmem_alloc(smem_u32(&s.tmem_base), kTmemCols);
     tmem_relinquish();
   }
+  __syncwarp();  // warps reach the CTA barrier converged (thread 0 alone did the setup)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -802,11 +807,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ------------------------------------------------------------ teardown
+  // Each warp reports the end of its role on roles_done once all its lanes
+  // are here (in the role warps one elected lane worked while the others went
+  // on), and the tensor memory is freed only after every report.  A CTA-wide
+  // __syncthreads reached by warps in that state was measured to release some
+  // warps microseconds before others had arrived, so it does not order this.
+  __syncwarp();
   tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 1) {
+  if (lane == 0) mbar_arrive(smem_u32(&s.roles_done));
+  if (warp == 4) {
+    // one lane polls (the others wait without taking issue slots)
+    if (lane == 0 && !mbar_wait(smem_u32(&s.roles_done), 0, nullptr, kWaitBudgetNs))
+      report(prm.dev_status, MLA_ERR_DEVICE_TIMEOUT);
     __syncwarp();
+    tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
 }
