@@ -78,10 +78,6 @@ struct __align__(1024) Smem {
   // in one phase.  No warp gets two tiles ahead (S of tile g+2 waits for the
   // P V of tile g), so two barriers suffice.
   uint64_t s_full[2], p_full[2], pv_done[2];
-  // P V of that buffer's tile issued: the tensor pipe runs MMAs in issue
-  // order, so the next S MMAs into the buffer may be issued behind it (the
-  // fences around the barrier order the two issuers' MMAs).
-  uint64_t pv_issued[2];
   // S MMAs of tile g all issued: the two S issuers take turns tile by tile, so
   // the pipe finishes one tile's S before the next (its softmax, P V and the
   // S-buffer reuse two tiles on depend on it) instead of interleaving both.
@@ -223,7 +219,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&s.s_full[i]), 1);
       mbar_init(smem_u32(&s.p_full[i]), kSoftmaxThreads);
       mbar_init(smem_u32(&s.pv_done[i]), 1);
-      mbar_init(smem_u32(&s.pv_issued[i]), 1);
       mbar_init(smem_u32(&s.qk_seq[i]), 1);
     }
     mbar_init(smem_u32(&s.qown_full), 1);
@@ -461,10 +456,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          // the S buffer may be overwritten behind P V of tile g-2 (which reads
-          // P from it): that P V must have been issued
+          // The S buffer is overwritten only once the P V of tile g-2, which
+          // reads P from it, has completed.  Issued is not enough: MMAs issued
+          // by different threads are not run in issue order (with only the
+          // issue ordered, through a barrier and the tcgen05 fences around it,
+          // P V read S values in place of P, a few heads per tile in ~97% of
+          // runs of a 64 x 4096 layer).
           if (!mbar_wait(smem_u32(&s.other_full[slot]), ph, abort_flag, kWaitBudgetNs) ||
-              (g >= 2 && !mbar_wait(smem_u32(&s.pv_issued[g & 1u]), ((g >> 1) - 1) & 1u,
+              (g >= 2 && !mbar_wait(smem_u32(&s.pv_done[g & 1u]), ((g >> 1) - 1) & 1u,
                                     abort_flag, kWaitBudgetNs))) {
             set_abort(s, prm.dev_status);
             ok = false;
@@ -538,8 +537,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kt = 0; kt < ksteps; ++kt)
             mma_ts(tmem + kColO, a_p + kt * 8, bw + (uint64_t)((kt * 2048) >> 4), id_pv,
                    (tt > t0 || kt > 0) ? 1u : 0u);
-          tc_fence_before();
-          mbar_arrive(smem_u32(&s.pv_issued[g & 1u]));
           mma_commit(smem_u32(&s.pv_done[g & 1u]));
           mma_commit(smem_u32(&s.own_empty[slot]));
         }
@@ -549,77 +546,90 @@ __global__ void __launch_bounds__(kThreads, 1)
         report(prm.dev_status, MLA_ERR_DEVICE_TIMEOUT);
     }
   } else if (warp == 9) {
-    // ------------------------------------------------------------ appended rows
-    // With kv_new, request b's newest row (token seq_len[b] - 1) is stored
-    // into its slot by the CTAs whose range holds that token, before their
-    // producers load the tile holding it: the warp writes the rows, orders
-    // them before the async proxy's reads, and signals row_ready.  Both CTAs
-    // of the pair store the same bytes, each before its own loads.
-    if (active && prm.kv_new) {
-      SegIter it;
-      it.init(v, prm.batch, pair, seg_n, seg_first);
-      int32_t t0, t1, slot_p;
-      while (it.next(t0, t1, slot_p)) {
-        const int32_t L = v.seq_len[it.b];
-        if (t1 != L || L == 0) continue;  // not the request's last segment
-        const int32_t pos = L - 1;
-        const int32_t blk = prm.block_table[(int64_t)it.b * prm.max_blocks_per_seq + pos / BS];
-        if (blk < 0 || blk >= prm.num_blocks) {
-          if (lane == 0) report(prm.dev_status, MLA_ERR_DEVICE_RANGE);
-          continue;
-        }
-        const int64_t row = (int64_t)blk * BS + pos % BS;
-        const uint4 *src = prm.kv_new + (int64_t)it.b * (kRow / 8);
-        uint4 *dst = prm.cache_rows + row * (kRow / 8);
-        for (int k = lane; k < kRow / 8; k += 32) dst[k] = __ldg(src + k);
-      }
-      fence_proxy_async_global();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&s.row_ready));
-    }
-    // ------------------------------------------------------------ Q loader
+    // ------------------------------------------------------------ Q loader and appended rows
     // Q of every segment's request, once the previous segment's S MMAs are
     // done with the Q buffers: first its own 256 dims (and rope), from where
     // the even S issuer copies the own dims into tensor memory (tcgen05.cp),
     // then, once copied, its other 256 dims.  A warp of its own, so that the
     // tile loads never wait behind Q.
-    if (active && elect_one_sync()) {
-      SegIter it;
-      it.init(v, prm.batch, pair, seg_n, seg_first);
-      int32_t t0, t1, slot_p;
+    //
+    // With kv_new, request b's newest row (token seq_len[b] - 1) is stored
+    // into its slot by the CTAs whose range holds that token, before their
+    // producers load the tile holding it: the warp writes the rows, orders
+    // them before the async proxy's reads, and signals row_ready.  Both CTAs
+    // of the pair store the same bytes, each before its own loads.  The first
+    // segment's Q goes out before these stores, whose table lookups are
+    // dependent loads: the first S MMAs need Q, while the newest row is
+    // usually needed tiles later.
+    if (active) {
+      const bool leader = elect_one_sync();
+      SegIter qi;
+      qi.init(v, prm.batch, pair, seg_n, seg_first);
+      int32_t qt0, qt1, qslot;
       uint32_t seg = 0;
-      prefetch_tmap(&maps.q);
-      while (it.next(t0, t1, slot_p)) {
+      bool qok = true;
+      // one segment's Q loads; false when a wait gave up
+      auto load_q = [&]() -> bool {
         if (!mbar_wait(smem_u32(&s.q_free), (seg & 1u) ^ 1u, abort_flag, kWaitBudgetNs)) {
           set_abort(s, prm.dev_status);
-          break;
+          return false;
         }
         // own dims: into the rings' slot 1 for the first segment (empty until
         // the copy is done, so Q's other dims need not wait), else the Q buffers
         mbar_arrive_expect_tx(smem_u32(&s.qown_full), 5 * kQChunkBytes);
         for (int c = 0; c < 4; ++c)
           tma_load_2d(smem_u32(seg == 0 ? q_stage_chunk(s, c) : s.q_other[c]), &maps.q,
-                      64 * (own0 + c), it.b * kHeads, smem_u32(&s.qown_full));
-        tma_load_2d(smem_u32(s.q_rope), &maps.q, 512, it.b * kHeads, smem_u32(&s.qown_full));
+                      64 * (own0 + c), qi.b * kHeads, smem_u32(&s.qown_full));
+        tma_load_2d(smem_u32(s.q_rope), &maps.q, 512, qi.b * kHeads, smem_u32(&s.qown_full));
         {  // the next segment's Q rows into L2 meanwhile
-          SegIter nx = it;
+          SegIter nx = qi;
           int32_t a0, a1, aslot;
           if (nx.next(a0, a1, aslot))
             for (int c = 0; c < 9; ++c) tma_prefetch_2d(&maps.q, 64 * c, nx.b * kHeads);
         }
         if (seg > 0 && !mbar_wait(smem_u32(&s.q_tmem), seg & 1u, abort_flag, kWaitBudgetNs)) {
           set_abort(s, prm.dev_status);
-          break;
+          return false;
         }
         mbar_arrive_expect_tx(smem_u32(&s.q_full), 4 * kQChunkBytes);
         for (int c = 0; c < 4; ++c)
-          tma_load_2d(smem_u32(s.q_other[c]), &maps.q, 64 * (oth0 + c), it.b * kHeads,
+          tma_load_2d(smem_u32(s.q_other[c]), &maps.q, 64 * (oth0 + c), qi.b * kHeads,
                       smem_u32(&s.q_full));
         ++seg;
+        return true;
+      };
+      // the first segment's Q (its waits pass at once)
+      if (leader && qi.next(qt0, qt1, qslot)) qok = load_q();
+      __syncwarp();
+      if (prm.kv_new) {
+        SegIter it;
+        it.init(v, prm.batch, pair, seg_n, seg_first);
+        int32_t t0, t1, slot_p;
+        while (it.next(t0, t1, slot_p)) {
+          const int32_t L = v.seq_len[it.b];
+          if (t1 != L || L == 0) continue;  // not the request's last segment
+          const int32_t pos = L - 1;
+          const int32_t blk = prm.block_table[(int64_t)it.b * prm.max_blocks_per_seq + pos / BS];
+          if (blk < 0 || blk >= prm.num_blocks) {
+            if (lane == 0) report(prm.dev_status, MLA_ERR_DEVICE_RANGE);
+            continue;
+          }
+          const int64_t row = (int64_t)blk * BS + pos % BS;
+          const uint4 *src = prm.kv_new + (int64_t)it.b * (kRow / 8);
+          uint4 *dst = prm.cache_rows + row * (kRow / 8);
+          for (int k = lane; k < kRow / 8; k += 32) dst[k] = __ldg(src + k);
+        }
+        fence_proxy_async_global();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&s.row_ready));
       }
-      if (s.abort) {  // let the last issued loads land before exit
-        (void)mbar_wait(smem_u32(&s.qown_full), 0, nullptr, kDrainBudgetNs);
-        (void)mbar_wait(smem_u32(&s.q_full), 0, nullptr, kDrainBudgetNs);
+      if (leader) {
+        // later segments' Q, each after the previous segment's S MMAs
+        while (qok && qi.next(qt0, qt1, qslot)) qok = load_q();
+        if (s.abort) {  // let the last issued loads land before exit
+          (void)mbar_wait(smem_u32(&s.qown_full), 0, nullptr, kDrainBudgetNs);
+          (void)mbar_wait(smem_u32(&s.q_full), 0, nullptr, kDrainBudgetNs);
+        }
       }
     }
   } else if (warp >= 4 && warp < 8) {

@@ -389,6 +389,31 @@ def test_config4_every_short_request_repeated(mla, q_kind):
         assert torch.equal(lse2, lse), f"repeat {rep} lse"
 
 
+def test_config2_layer_repeated_bit_identical(mla):
+    """A 64 x 4096 layer decoded thirty times: every output finite and equal
+    bit for bit to the first.  Its ranges hold long runs of tiles, where the
+    S MMAs two tiles on overwrite the tensor-memory buffer that P V reads P
+    from; an S issued before that P V has finished shows up as a few heads of
+    non-finite or changing output (P read from raw fp32 S bits)."""
+    w = mi.workload(2)
+    dl = mi.make_device_layer(w, 0, "cuda", q_kind="sharp")
+    ws = mla.make_workspace(w.batch)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.mla_cache_append(dl["kv_new"], dl["slot_mapping"], dl["cache"], dev_status=status)
+    first = None
+    for rep in range(30):
+        out = torch.full((w.batch, 128, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+        mla.mla_decode(dl["q"], dl["cache"], dl["block_table"], dl["seq_lens"],
+                       dl["softmax_scale"], out, None, workspace=ws, dev_status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert bool(torch.isfinite(out.float()).all()), f"run {rep}: non-finite output"
+        if first is None:
+            first = out
+        else:
+            assert torch.equal(out.view(torch.int16), first.view(torch.int16)), f"run {rep} differs"
+
+
 def test_partial_then_combine_equals_planned(mla):
     """mla_decode_partial + mla_combine_planned is exactly mla_decode_planned."""
     w = mi.workload(4)
