@@ -644,3 +644,76 @@ def test_graph_captured_step_equals_eager(mla):
         ref, ref_lse = _oracle_sample(host, reqs)
         assert_close(host_f64(o)[reqs], ref, "graph step")
         assert_lse_close(l.cpu().numpy()[reqs], ref_lse)
+
+
+def _read_plan(ws, batch):
+    """The plan in the workspace, parsed with the layout documented next to
+    the planner (all offsets 256-byte aligned)."""
+    raw = ws.cpu().numpy().view(np.uint8)
+    a256 = lambda x: (x + 255) & ~255
+    hdr = raw[:32].view(np.int32)
+    U, P, Pm = int(hdr[0]), int(hdr[1]), int(hdr[2])
+    o = a256(32)
+    seq = raw[o:o + 4 * batch].view(np.int32); o = a256(o + 4 * batch)
+    prefix = raw[o:o + 4 * (batch + 1)].view(np.int32); o = a256(o + 4 * (batch + 1))
+    rstart = raw[o:o + 4 * (Pm + 1)].view(np.int32); o = a256(o + 4 * (Pm + 1))
+    o = a256(o + 4 * (Pm + 1))            # range_first
+    o = a256(o + 8 * (batch + 1))         # cost_prefix
+    o = a256(o + 4 * 2 * batch)           # counters
+    segc = raw[o:o + 4 * Pm].view(np.int32); o = a256(o + 4 * Pm)
+    recs = raw[o:o + 32 * 4 * Pm].view(np.int32).reshape(Pm, 4, 8); o = a256(o + 32 * 4 * Pm)
+    split = raw[o:o + 16 * batch].view(np.int32).reshape(batch, 4)
+    return dict(U=U, P=P, Pm=Pm, seq=seq, prefix=prefix, rstart=rstart, segc=segc, recs=recs,
+                split=split)
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_plan_invariants(mla, cfg):
+    """The planner's ranges tile the units; every range's segment records,
+    every request's split record and the partial slots follow from the
+    ranges; and the ranges' modelled costs (2 per unit, 7 per request start,
+    a start counted in the range holding the request's first unit) are
+    balanced: the targets are C/P apart and a boundary lands within a start's
+    cost or a unit of its target, so no two ranges differ by more than
+    2 x (7 + 2)."""
+    w = mi.workload(cfg)
+    dl = mi.make_device_layer(w, 0, "cuda")
+    ws = mla.make_workspace(w.batch)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.mla_decode_plan(dl["seq_lens"], dl["block_table"], w.block_size, ws, dev_status=status,
+                        num_blocks=dl["cache"].shape[0])
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    pl = _read_plan(ws, w.batch)
+    unit = 64
+    seq = dl["seq_lens"].cpu().numpy().astype(np.int64)
+    units = (seq + unit - 1) // unit
+    assert np.array_equal(pl["seq"], seq)
+    assert np.array_equal(pl["prefix"], np.concatenate([[0], np.cumsum(units)]))
+    U, P, R = pl["U"], pl["P"], pl["rstart"].astype(np.int64)
+    assert U == units.sum() and P == min(U, pl["Pm"])
+    assert R[0] == 0 and R[P] == U and np.all(np.diff(R[:P + 1]) > 0) and np.all(R[P:] == U)
+    starts = pl["prefix"][:-1][units > 0]
+    cost = []
+    for p in range(P):
+        r0, r1 = R[p], R[p + 1]
+        segs = []
+        for b in range(w.batch):
+            Ub, Ue = pl["prefix"][b], pl["prefix"][b + 1]
+            u0, u1 = max(r0, Ub), min(r1, Ue)
+            if u0 < u1:
+                slot = (2 * p + (1 if r0 < Ub else 0)) if (Ub < r0 or Ue > r1) else -1
+                segs.append((b, (u0 - Ub) * unit, min((u1 - Ub) * unit, seq[b]), slot))
+        assert pl["segc"][p] == len(segs)
+        for i, sgm in enumerate(segs[:4]):
+            assert tuple(pl["recs"][p, i, :4]) == sgm, (p, i)
+        cost.append(2 * (r1 - r0) + 7 * int(((starts >= r0) & (starts < r1)).sum()))
+    for b in range(w.batch):
+        if units[b] == 0:
+            continue
+        Ub, Ue = pl["prefix"][b], pl["prefix"][b + 1]
+        p0 = int(np.searchsorted(R[:P], Ub, side="right") - 1)
+        p1 = int(np.searchsorted(R[:P], Ue - 1, side="right") - 1)
+        assert tuple(pl["split"][b, :3]) == (p0, p1, 1 if R[p0] < Ub else 0), b
+    if U >= 8 * P:  # ranges of several units
+        assert max(cost) - min(cost) <= 2 * (7 + 2), (min(cost), max(cost))
