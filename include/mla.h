@@ -282,6 +282,55 @@ mla_status_t mla_decode_noalloc(const void *q, const void *cache, int64_t num_bl
                                 float softmax_scale, void *out, float *lse, int32_t *dev_status,
                                 void *stream);
 
+/*
+ * mla_place_requests — KV-load-aware placement of requests on data-parallel
+ * attention ranks (host only; no GPU, no CUDA call).
+ *
+ * Under DP attention every rank decodes its own requests, and the MoE
+ * all-to-all that follows attention keeps the ranks in lockstep, so a step
+ * lasts as long as the rank with the most cache to read.  A rank holding the
+ * long-context requests slows every rank, and long requests have to be
+ * spread over the ranks [dp-attention-expert-parallel-mla-kv-replication
+ * (inferenceinterviews.com), "What it costs" and "What interviewers probe
+ * next"].  A decode reads every cached latent row of a request, so a rank's
+ * load is the sum of its requests' cached tokens.
+ *
+ * Requests are placed longest first (ties: lower index first), each on the
+ * rank with the least load so far (ties: lower rank), provided that rank's
+ * load plus the request stays within capacity_tokens (0: no limit).  When
+ * the least loaded rank cannot take it, no rank can, and the request is left
+ * unplaced (rank_of = -1).  This is list scheduling in decreasing order
+ * (Graham 1969): with no capacity limit the largest load is at most
+ * (4/3 - 1/(3 ranks)) times the smallest achievable.
+ *
+ *   kv_tokens   host int64 [n]: cached tokens of request i (>= 0)
+ *   n           number of requests (>= 0; 0 places nothing)
+ *   ranks       number of DP ranks (>= 1)
+ *   capacity_tokens  per-rank limit on the load (>= 0; 0: none)
+ *   rank_of     host int32 [n], written: the rank of request i, or -1
+ *   rank_load   host int64 [ranks], written: each rank's load
+ *   unplaced    host int32, nullable: written with the number of -1 entries
+ *
+ * Returns MLA_OK, or MLA_ERR_INVALID_ARGUMENT (n < 0, ranks < 1, a negative
+ * length or capacity, or a null array that is needed) with nothing written.
+ * The caller owns every array; the library keeps nothing.
+ */
+mla_status_t mla_place_requests(const int64_t *kv_tokens, int32_t n, int32_t ranks,
+                                int64_t capacity_tokens, int32_t *rank_of, int64_t *rank_load,
+                                int32_t *unplaced);
+
+/*
+ * mla_place_one — the online form: the rank a new request of kv_tokens cached
+ * tokens goes to, given the ranks' current loads (the least loaded, ties:
+ * lower rank), or -1 in *rank when that rank's load plus the request exceeds
+ * capacity_tokens (0: no limit).  rank_load is not changed.
+ *
+ * Returns MLA_OK, or MLA_ERR_INVALID_ARGUMENT (ranks < 1, a null pointer, a
+ * negative length, load or capacity).
+ */
+mla_status_t mla_place_one(const int64_t *rank_load, int32_t ranks, int64_t capacity_tokens,
+                           int64_t kv_tokens, int32_t *rank);
+
 #ifdef __cplusplus
 }
 #endif

@@ -29,7 +29,7 @@ STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARGUMENT", 2: "MLA_ERR_UNSUPPORTED",
 EXPORTED = ("mla_status_string", "mla_last_error_detail", "mla_abi_version", "mla_cache_append",
             "mla_decode_workspace_size", "mla_decode_plan", "mla_decode", "mla_decode_planned",
             "mla_combine", "mla_decode_noalloc", "mla_decode_partial", "mla_combine_planned",
-            "mla_decode_append_planned")
+            "mla_decode_append_planned", "mla_place_requests", "mla_place_one")
 
 
 class MlaError(RuntimeError):
@@ -75,6 +75,10 @@ def _load():
     lib.mla_combine.restype = ctypes.c_int
     lib.mla_decode_noalloc.argtypes = [P, P, i64, i32, P, i32, P, i32, i32, i32, f32, P, P, P, P]
     lib.mla_decode_noalloc.restype = ctypes.c_int
+    lib.mla_place_requests.argtypes = [P, i32, i32, i64, P, P, P]
+    lib.mla_place_requests.restype = ctypes.c_int
+    lib.mla_place_one.argtypes = [P, i32, i64, i64, P]
+    lib.mla_place_one.restype = ctypes.c_int
     return lib
 
 
@@ -293,3 +297,33 @@ def mla_decode_noalloc(q, cache, block_table, seq_lens, softmax_scale, out, lse=
         block_table.shape[1], _ptr(seq_lens), B, H, int(max_seq_len), float(softmax_scale),
         _ptr(out), _ptr(lse), _ptr(dev_status), _stream(stream)))
     return out
+
+
+def place_requests(kv_tokens, ranks: int, capacity_tokens: int = 0):
+    """KV-load-aware placement of requests on `ranks` DP attention ranks
+    (mla_place_requests; host only).  kv_tokens: cached tokens per request.
+    Returns (rank_of int32 [n], -1 where no rank can hold the request within
+    capacity_tokens; rank_load int64 [ranks])."""
+    import numpy as np
+    t = np.ascontiguousarray(kv_tokens, dtype=np.int64)
+    if t.ndim != 1:
+        raise ValueError("kv_tokens must be 1-D")
+    rank_of = np.empty(t.shape[0], np.int32)
+    rank_load = np.empty(int(ranks), np.int64)
+    unplaced = ctypes.c_int32(0)
+    _check(get_lib().mla_place_requests(t.ctypes.data if t.size else None, t.shape[0], int(ranks),
+                                        int(capacity_tokens),
+                                        rank_of.ctypes.data if t.size else None,
+                                        rank_load.ctypes.data, ctypes.byref(unplaced)))
+    return rank_of, rank_load
+
+
+def place_one(rank_load, kv_tokens: int, capacity_tokens: int = 0) -> int:
+    """The rank a new request of kv_tokens cached tokens goes to, given the
+    ranks' loads (mla_place_one; host only), or -1 if none can hold it."""
+    import numpy as np
+    lo = np.ascontiguousarray(rank_load, dtype=np.int64)
+    rank = ctypes.c_int32(0)
+    _check(get_lib().mla_place_one(lo.ctypes.data, lo.shape[0], int(capacity_tokens),
+                                   int(kv_tokens), ctypes.byref(rank)))
+    return rank.value

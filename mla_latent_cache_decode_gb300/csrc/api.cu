@@ -115,6 +115,10 @@ mla_status_t check_decode_args(const void *q, const void *cache, int64_t num_blo
 // Failure reporting for the fixed-scratch entry point (noalloc.cu).
 mla_status_t noalloc_fail(mla_status_t s, const char *msg) { return fail(s, "%s", msg); }
 
+// The thread's error detail (read by mla_last_error_detail), for the host-only
+// entry points of placement.cu.
+void set_error_detail(const char *msg) { g_detail = msg ? msg : ""; }
+
 }  // namespace mla
 
 using namespace mla;
