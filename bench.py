@@ -415,12 +415,59 @@ def run_mine(args, w, rank, world, local_rank):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
+    if not args.no_absorption:
+        result["absorption"] = measure_absorption(w, device, stream, hbm_peak)
     if not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, W, budget_s=args.cpu_budget)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
     return result
+
+
+def measure_absorption(w, device, stream, hbm_peak, reps=20):
+    """The absorption GEMMs of the same layers, timed beside the step (not in
+    it): per layer q = [q_nope . W_UK ; q_pe] and o = out . W_UV over the
+    rank's batch, each layer with its own random bf16 weights (33.6 MB a layer:
+    the step streams them from HBM once, as a model does)."""
+    import torch
+    import mla_latent_cache_decode_gb300 as mla
+    L, B = w.layers, w.batch
+    g = torch.Generator(device=device).manual_seed(20261202)
+    bf = torch.bfloat16
+    w_uk = [torch.randn((128, 128, 512), generator=g, device=device).mul_(128 ** -0.5).to(bf)
+            for _ in range(L)]
+    w_uv = [torch.randn((128, 512, 128), generator=g, device=device).mul_(512 ** -0.5).to(bf)
+            for _ in range(L)]
+    q_nope = torch.randn((B, 128, 128), generator=g, device=device).to(bf)
+    q_pe = torch.randn((B, 128, 64), generator=g, device=device).to(bf)
+    out = torch.randn((B, 128, 512), generator=g, device=device).to(bf)
+    q = torch.empty((B, 128, mi.ROW), dtype=bf, device=device)
+    o = torch.empty((B, 128, 128), dtype=bf, device=device)
+    sh = stream.cuda_stream
+
+    def layers():
+        for l in range(L):
+            mla.mla_absorb_q(q_nope, q_pe, w_uk[l], q, stream=sh)
+            mla.mla_absorb_out(out, w_uv[l], o, stream=sh)
+
+    for _ in range(3):
+        layers()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        layers()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us_layer = e0.elapsed_time(e1) * 1e3 / (reps * L)
+    per_layer = 2 * (128 * 128 * 512 * 2) + B * 128 * (128 + 64 + 576 + 512 + 128) * 2
+    gbs = per_layer / (us_layer * 1e-6) / 1e9
+    return {"what": "q = [q_nope . W_UK ; q_pe] and o = out . W_UV per layer (cuBLAS batched "
+                    "GEMMs over 128 heads), not part of the step's value",
+            "us_per_layer": round(us_layer, 2), "us_per_step": round(us_layer * L, 1),
+            "bytes_per_layer": per_layer, "achieved_gbs": round(gbs, 1),
+            "frac_of_hbm_peak": round(gbs / hbm_peak, 4), "launches_per_layer": 3}
 
 
 # ----------------------------------------------------------------------------- oracle on the host
@@ -510,6 +557,8 @@ def main():
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-absorption", action="store_true",
+                    help="skip the separate timing of the absorption GEMMs")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--layers", type=int, default=0,
                     help="run only the first N layers of the workload (for profiling captures)")

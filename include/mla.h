@@ -283,6 +283,39 @@ mla_status_t mla_decode_noalloc(const void *q, const void *cache, int64_t num_bl
                                 void *stream);
 
 /*
+ * mla_absorb_q / mla_absorb_out — the absorption GEMMs on either side of the
+ * absorbed-form decode.  In decode each head's query is projected into the
+ * latent space and the head attends over the shared latent directly
+ * [dp-attention-expert-parallel-mla-kv-replication (inferenceinterviews.com),
+ * "A strong answer"]; the head's 128 non-rotary query dims and its 128 value
+ * dims map to the 512-dim latent through W_UK and W_UV, and the 64 rotary
+ * dims are shared [MLA 的 TP 切分 (10100.com), §2.2].
+ *
+ * mla_absorb_q:   q[b,h,0:512]   = q_nope[b,h,:] . W_UK[h]   (fp32 sums)
+ *                 q[b,h,512:576] = q_pe[b,h,:]                (copied)
+ *   q_nope  device bf16 [B, 128, 128]   w_uk device bf16 [128, 128, 512]
+ *   q_pe    device bf16 [B, 128, 64]    q    device bf16 [B, 128, 576], written
+ * mla_absorb_out: o[b,h,:] = out[b,h,:] . W_UV[h]             (fp32 sums)
+ *   out     device bf16 [B, 128, 512]   w_uv device bf16 [128, 512, 128]
+ *   o       device bf16 [B, 128, 128], written
+ *
+ * All row-major and contiguous, 16-byte aligned; num_heads must be 128.  Both
+ * are batched GEMMs over the heads on cuBLAS, enqueued on `stream`.  The first
+ * call on a device creates a cuBLAS handle and a 32 MiB workspace for it,
+ * kept until exit (the only device memory the library allocates): make that
+ * first call before any stream capture.  Calls on one device are serialised
+ * on its handle.
+ *
+ * Returns MLA_OK (B = 0: nothing enqueued), MLA_ERR_INVALID_ARGUMENT
+ * (B < 0, null or misaligned pointers), MLA_ERR_UNSUPPORTED (num_heads), or
+ * MLA_ERR_CUDA.
+ */
+mla_status_t mla_absorb_q(const void *q_nope, const void *q_pe, const void *w_uk, int32_t batch,
+                          int32_t num_heads, void *q, void *stream);
+mla_status_t mla_absorb_out(const void *out, const void *w_uv, int32_t batch, int32_t num_heads,
+                            void *o, void *stream);
+
+/*
  * mla_place_requests — KV-load-aware placement of requests on data-parallel
  * attention ranks (host only; no GPU, no CUDA call).
  *

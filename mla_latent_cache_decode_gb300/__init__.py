@@ -29,7 +29,8 @@ STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARGUMENT", 2: "MLA_ERR_UNSUPPORTED",
 EXPORTED = ("mla_status_string", "mla_last_error_detail", "mla_abi_version", "mla_cache_append",
             "mla_decode_workspace_size", "mla_decode_plan", "mla_decode", "mla_decode_planned",
             "mla_combine", "mla_decode_noalloc", "mla_decode_partial", "mla_combine_planned",
-            "mla_decode_append_planned", "mla_place_requests", "mla_place_one")
+            "mla_decode_append_planned", "mla_place_requests", "mla_place_one", "mla_absorb_q",
+            "mla_absorb_out")
 
 
 class MlaError(RuntimeError):
@@ -79,6 +80,10 @@ def _load():
     lib.mla_place_requests.restype = ctypes.c_int
     lib.mla_place_one.argtypes = [P, i32, i64, i64, P]
     lib.mla_place_one.restype = ctypes.c_int
+    lib.mla_absorb_q.argtypes = [P, P, P, i32, i32, P, P]
+    lib.mla_absorb_q.restype = ctypes.c_int
+    lib.mla_absorb_out.argtypes = [P, P, i32, i32, P, P]
+    lib.mla_absorb_out.restype = ctypes.c_int
     return lib
 
 
@@ -327,3 +332,33 @@ def place_one(rank_load, kv_tokens: int, capacity_tokens: int = 0) -> int:
     _check(get_lib().mla_place_one(lo.ctypes.data, lo.shape[0], int(capacity_tokens),
                                    int(kv_tokens), ctypes.byref(rank)))
     return rank.value
+
+
+def mla_absorb_q(q_nope, q_pe, w_uk, q, stream=None):
+    """q[b,h,0:512] = q_nope[b,h] . W_UK[h]; q[b,h,512:576] = q_pe[b,h] (mla_absorb_q)."""
+    import torch
+    _need(q_nope, torch.bfloat16, 3, "q_nope")
+    _need(q_pe, torch.bfloat16, 3, "q_pe")
+    _need(w_uk, torch.bfloat16, 3, "w_uk")
+    _need(q, torch.bfloat16, 3, "q")
+    B, H = q_nope.shape[0], q_nope.shape[1]
+    if (tuple(q_nope.shape) != (B, H, 128) or tuple(q_pe.shape) != (B, H, 64)
+            or tuple(w_uk.shape) != (H, 128, 512) or tuple(q.shape) != (B, H, ROW_DIM)):
+        raise ValueError("shapes: q_nope [B,H,128], q_pe [B,H,64], w_uk [H,128,512], q [B,H,576]")
+    _check(get_lib().mla_absorb_q(_ptr(q_nope), _ptr(q_pe), _ptr(w_uk), B, H, _ptr(q),
+                                  _stream(stream)))
+    return q
+
+
+def mla_absorb_out(out, w_uv, o, stream=None):
+    """o[b,h] = out[b,h] . W_UV[h] (mla_absorb_out)."""
+    import torch
+    _need(out, torch.bfloat16, 3, "out")
+    _need(w_uv, torch.bfloat16, 3, "w_uv")
+    _need(o, torch.bfloat16, 3, "o")
+    B, H = out.shape[0], out.shape[1]
+    if (tuple(out.shape) != (B, H, 512) or tuple(w_uv.shape) != (H, 512, 128)
+            or tuple(o.shape) != (B, H, 128)):
+        raise ValueError("shapes: out [B,H,512], w_uv [H,512,128], o [B,H,128]")
+    _check(get_lib().mla_absorb_out(_ptr(out), _ptr(w_uv), B, H, _ptr(o), _stream(stream)))
+    return o

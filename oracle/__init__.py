@@ -152,3 +152,28 @@ def bf16_bits_to_f64(bits) -> np.ndarray:
     """Exact widening of bfloat16 bit patterns to fp64."""
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
     return b.view(np.float32).astype(np.float64)
+
+
+def absorb_q(q_nope, q_pe, w_uk) -> np.ndarray:
+    """The absorbed query in fp64: q[b,h,0:512] = sum_i q_nope[b,h,i] W_UK[h,i,:],
+    q[b,h,512:576] = q_pe[b,h,:].  Each head's non-rotary query is projected
+    into the latent space, the rotary dims are shared as they are
+    [dp-attention-expert-parallel-mla-kv-replication (inferenceinterviews.com),
+    "A strong answer"; MLA 的 TP 切分 (10100.com), section 一].
+
+    q_nope [B,H,128], q_pe [B,H,64], w_uk [H,128,512]: bfloat16 bit patterns.
+    Returns [B,H,576] fp64."""
+    qn = bf16_bits_to_f64(q_nope)
+    w = bf16_bits_to_f64(w_uk)
+    lat = np.einsum("bhi,hik->bhk", qn, w)
+    return np.concatenate([lat, bf16_bits_to_f64(q_pe)], axis=2)
+
+
+def absorb_out(out, w_uv) -> np.ndarray:
+    """The head's value output in fp64: o[b,h,:] = sum_k out[b,h,k] W_UV[h,k,:]
+    (same passages as absorb_q).  out [B,H,512]: fp64 values, or bfloat16 bit
+    patterns (uint16); w_uv [H,512,128]: bfloat16 bit patterns.  Returns
+    [B,H,128] fp64."""
+    out = np.asarray(out)
+    o = bf16_bits_to_f64(out) if out.dtype == np.uint16 else out.astype(np.float64)
+    return np.einsum("bhk,hkj->bhj", o, bf16_bits_to_f64(w_uv))

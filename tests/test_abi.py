@@ -70,3 +70,21 @@ def test_host_validation_before_any_launch(lib):
     assert lib.mla_cache_append(None, None, -1, None, 1, 16, None, None) == 1
     assert lib.mla_combine(None, None, None, 0, 128, None, None, None) == 0
     assert lib.mla_combine(None, None, None, 2, 128, None, None, None) == 1
+
+
+def test_absorption_host_validation(lib):
+    P, i32 = ctypes.c_void_p, ctypes.c_int32
+    lib.mla_absorb_q.argtypes = [P, P, P, i32, i32, P, P]
+    lib.mla_absorb_q.restype = ctypes.c_int
+    lib.mla_absorb_out.argtypes = [P, P, i32, i32, P, P]
+    lib.mla_absorb_out.restype = ctypes.c_int
+    lib.mla_last_error_detail.restype = ctypes.c_char_p
+    assert lib.mla_absorb_q(None, None, None, 0, 128, None, None) == 0     # empty batch: no-op
+    assert lib.mla_absorb_q(None, None, None, -1, 128, None, None) == 1
+    assert lib.mla_absorb_q(None, None, None, 4, 64, None, None) == 2      # heads other than 128
+    assert lib.mla_absorb_q(None, None, None, 4, 128, None, None) == 1     # null pointers
+    assert b"null" in lib.mla_last_error_detail()
+    assert lib.mla_absorb_q(16, 32, 48, 4, 128, 72, None) == 1             # misaligned
+    assert lib.mla_absorb_out(None, None, 0, 128, None, None) == 0
+    assert lib.mla_absorb_out(None, None, 4, 128, None, None) == 1
+    assert lib.mla_absorb_out(None, None, 4, 100, None, None) == 2

@@ -717,3 +717,63 @@ def test_plan_invariants(mla, cfg):
         assert tuple(pl["split"][b, :3]) == (p0, p1, 1 if R[p0] < Ub else 0), b
     if U >= 8 * P:  # ranges of several units
         assert max(cost) - min(cost) <= 2 * (7 + 2), (min(cost), max(cost))
+
+
+# ------------------------------------------------------------ absorption GEMMs
+
+def _absorb_inputs(B, seed):
+    rng = np.random.default_rng(seed)
+
+    def bf16(shape, s=1.0):
+        return mi.f32_to_bf16_bits((rng.standard_normal(shape) * s).astype(np.float32))
+    return dict(q_nope=bf16((B, 128, 128)), q_pe=bf16((B, 128, 64)),
+                w_uk=bf16((128, 128, 512), 128 ** -0.5), w_uv=bf16((128, 512, 128), 512 ** -0.5),
+                out=bf16((B, 128, 512)))
+
+
+@pytest.mark.parametrize("B", [1, 20, 64])
+def test_absorb_q_matches_oracle(mla, B):
+    """q[b,h,:512] = q_nope[b,h] . W_UK[h] within the parity bar (fp32 sums, bf16
+    out); q[b,h,512:] = q_pe[b,h] bit for bit."""
+    x = _absorb_inputs(B, 100 + B)
+    q = torch.empty((B, 128, 576), dtype=torch.bfloat16, device="cuda")
+    mla.mla_absorb_q(dev_bf16(x["q_nope"]), dev_bf16(x["q_pe"]), dev_bf16(x["w_uk"]), q)
+    torch.cuda.synchronize()
+    ref = oracle.absorb_q(x["q_nope"], x["q_pe"], x["w_uk"])
+    assert_close(host_f64(q)[:, :, :512], ref[:, :, :512], f"absorbed q B={B}")
+    assert np.array_equal(host_bits(q)[:, :, 512:], x["q_pe"])
+
+
+@pytest.mark.parametrize("B", [1, 20, 64])
+def test_absorb_out_matches_oracle(mla, B):
+    """o[b,h] = out[b,h] . W_UV[h] within the parity bar."""
+    x = _absorb_inputs(B, 200 + B)
+    o = torch.empty((B, 128, 128), dtype=torch.bfloat16, device="cuda")
+    mla.mla_absorb_out(dev_bf16(x["out"]), dev_bf16(x["w_uv"]), o)
+    torch.cuda.synchronize()
+    assert_close(host_f64(o), oracle.absorb_out(x["out"], x["w_uv"]), f"absorbed out B={B}")
+
+
+def test_absorbed_layer_chain_matches_oracle(mla):
+    """q_nope, q_pe -> mla_absorb_q -> mla_decode -> mla_absorb_out against the
+    oracle's absorb_q -> decode -> absorb_out on the same inputs."""
+    lens = [1, 70, 513, 1500]
+    w = mi.custom_workload(lens, block_size=64, append=False, pool_factor=1.5)
+    dl = mi.make_device_layer(w, 0, "cuda")
+    B = len(lens)
+    x = _absorb_inputs(B, 300)
+    q = torch.empty((B, 128, 576), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((B, 128, 512), dtype=torch.bfloat16, device="cuda")
+    o = torch.empty((B, 128, 128), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.mla_absorb_q(dev_bf16(x["q_nope"]), dev_bf16(x["q_pe"]), dev_bf16(x["w_uk"]), q)
+    mla.mla_decode(q, dl["cache"], dl["block_table"], dl["seq_lens"], dl["softmax_scale"], out,
+                   workspace=mla.make_workspace(B), dev_status=status)
+    mla.mla_absorb_out(out, dev_bf16(x["w_uv"]), o)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    q_ref = oracle.absorb_q(x["q_nope"], x["q_pe"], x["w_uk"])
+    q_ref_bits = mi.f32_to_bf16_bits(q_ref.astype(np.float32))
+    out_ref, _ = oracle.decode(q_ref_bits, host_bits(dl["cache"]), dl["block_table_host"],
+                               np.array(lens, np.int32), dl["softmax_scale"])
+    assert_close(host_f64(o), oracle.absorb_out(out_ref, x["w_uv"]), "absorbed layer")

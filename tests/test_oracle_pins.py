@@ -62,6 +62,43 @@ def test_matches_nonabsorbed_mha(heads, lens):
         assert err < 1e-10, (b, err)
 
 
+@pytest.mark.parametrize("heads", [8, 128])
+def test_absorption_chain_matches_nonabsorbed_mha(heads):
+    """absorb_out(decode(absorb_q(q_nope, q_pe, W_UK)), W_UV) equals explicit-K/V
+    multi-head attention with keys [W_UK[h]^T c ; k_rope] and values
+    W_UV[h]^T c.  W_UK and q_nope are chosen so that the absorbed query is
+    exact in bfloat16 (entries in {-1,0,1} and {-1,0,1}/8); W_UV is any
+    bfloat16 array.  A transposed weight, a dropped rope copy or a wrong
+    contraction index in either absorption fails this by orders of magnitude."""
+    rng = np.random.default_rng(17)
+    lens, BS = [4, 29], 16
+    w = mi.custom_workload(lens, block_size=BS, append=False, pool_factor=2.0)
+    NB = w.num_blocks()
+    bt = mi.make_block_table(rng, lens, BS, NB)
+    cache = mi.f32_to_bf16_bits(rng.standard_normal((NB, BS, 576), dtype=np.float32))
+    mi.poison_unused(cache, bt, lens, BS)
+    B = len(lens)
+    w_uk_f = rng.choice([-1.0, 0.0, 1.0], p=[0.02, 0.96, 0.02], size=(heads, 128, 512))
+    q_nope_f = rng.choice([-1.0, 0.0, 1.0], size=(B, heads, 128)) / 8.0
+    w_uk = mi.f32_to_bf16_bits(w_uk_f.astype(np.float32))
+    q_nope = mi.f32_to_bf16_bits(q_nope_f.astype(np.float32))
+    q_pe = mi.f32_to_bf16_bits(rng.standard_normal((B, heads, 64), dtype=np.float32))
+    w_uv = mi.f32_to_bf16_bits(rng.standard_normal((heads, 512, 128), dtype=np.float32))
+    q = oracle.absorb_q(q_nope, q_pe, w_uk)
+    q_bits = mi.f32_to_bf16_bits(q.astype(np.float32))
+    assert np.array_equal(oracle.bf16_bits_to_f64(q_bits), q), "absorbed q not exact in bf16"
+    scale = 1.0 / math.sqrt(192.0)
+    out, _ = oracle.decode(q_bits, cache, bt, np.array(lens, np.int32), scale)
+    o = oracle.absorb_out(out, w_uv)
+    for b, L in enumerate(lens):
+        rows = oracle.bf16_bits_to_f64(mi.gather_rows(cache, bt, b, L, BS))
+        ref = nonabsorbed.mha_nonabsorbed(q_nope_f[b], oracle.bf16_bits_to_f64(q_pe[b]), w_uk_f,
+                                          oracle.bf16_bits_to_f64(w_uv).transpose(0, 2, 1),
+                                          rows, scale)
+        err = np.abs(o[b] - ref).max() / np.abs(ref).max()
+        assert err < 1e-10, (b, err)
+
+
 def test_matches_textbook_attention_per_head():
     """Each (b, h) equals softmax(scale K q) V with K = rows, V = rows[:, :512]."""
     w, d = _layer([1, 9, 40], heads=4, q_kind="sharp", seed=3)
