@@ -299,12 +299,10 @@ mla_status_t mla_decode_noalloc(const void *q, const void *cache, int64_t num_bl
  *   out     device bf16 [B, 128, 512]   w_uv device bf16 [128, 512, 128]
  *   o       device bf16 [B, 128, 128], written
  *
- * All row-major and contiguous, 16-byte aligned; num_heads must be 128.  Both
- * are batched GEMMs over the heads on cuBLAS, enqueued on `stream`.  The first
- * call on a device creates a cuBLAS handle and a 32 MiB workspace for it,
- * kept until exit (the only device memory the library allocates): make that
- * first call before any stream capture.  Calls on one device are serialised
- * on its handle.
+ * All row-major and contiguous, 16-byte aligned; num_heads must be 128; any
+ * B >= 0.  Each is one launch of a tensor-core kernel on `stream` (one CTA
+ * per head and column tile streams the head's weight through TMA); nothing is
+ * allocated and nothing is synchronised, so the calls can be captured.
  *
  * Returns MLA_OK (B = 0: nothing enqueued), MLA_ERR_INVALID_ARGUMENT
  * (B < 0, null or misaligned pointers), MLA_ERR_UNSUPPORTED (num_heads), or

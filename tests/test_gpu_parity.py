@@ -731,7 +731,7 @@ def _absorb_inputs(B, seed):
                 out=bf16((B, 128, 512)))
 
 
-@pytest.mark.parametrize("B", [1, 20, 64])
+@pytest.mark.parametrize("B", [1, 20, 64, 200])
 def test_absorb_q_matches_oracle(mla, B):
     """q[b,h,:512] = q_nope[b,h] . W_UK[h] within the parity bar (fp32 sums, bf16
     out); q[b,h,512:] = q_pe[b,h] bit for bit."""
@@ -744,7 +744,7 @@ def test_absorb_q_matches_oracle(mla, B):
     assert np.array_equal(host_bits(q)[:, :, 512:], x["q_pe"])
 
 
-@pytest.mark.parametrize("B", [1, 20, 64])
+@pytest.mark.parametrize("B", [1, 20, 64, 200])
 def test_absorb_out_matches_oracle(mla, B):
     """o[b,h] = out[b,h] . W_UV[h] within the parity bar."""
     x = _absorb_inputs(B, 200 + B)
