@@ -417,6 +417,8 @@ def run_mine(args, w, rank, world, local_rank):
     }
     if not args.no_absorption:
         result["absorption"] = measure_absorption(w, device, stream, hbm_peak)
+    if args.tp_compare:
+        result["tp_rank"] = measure_tp_rank(device, stream, hbm_peak, ms_step, L)
     if not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, W, budget_s=args.cpu_budget)
     if world > 1:
@@ -475,6 +477,65 @@ def measure_absorption(w, device, stream, hbm_peak, reps=20):
             "us_per_layer": round(us_layer, 2), "us_per_step": round(us_layer * L, 1),
             "bytes_per_layer": per_layer, "achieved_gbs": round(gbs, 1),
             "frac_of_hbm_peak": round(gbs / hbm_peak, 4), "launches_per_layer": 2}
+
+
+def measure_tp_rank(device, stream, hbm_peak, dp_ms_step, layers, distinct=4, reps=5):
+    """The same node batch under tensor-parallel attention (TP = 8): one rank
+    decodes all 159 x 4096 sequences for its 16 of the 128 heads, so it reads
+    the whole node's cache, against the DP rank's 20 sequences for all heads
+    [dp-attention-expert-parallel-mla-kv-replication (inferenceinterviews.com),
+    "A strong answer": 45.8 GB against 5.7 GB per step].  The step decodes
+    `layers` layers in a CUDA graph; their caches cycle through `distinct`
+    layers of 0.75 GB each (each far larger than L2, so every layer's cache is
+    read from HBM, as with 61 caches)."""
+    import torch
+    import mla_latent_cache_decode_gb300 as mla
+    heads, B, L_tok = 16, 159, 4096
+    w = mi.custom_workload([L_tok] * B, block_size=64, layers=distinct, append=False,
+                           pool_factor=1.0)
+    lay = [mi.make_device_layer(w, l, device, num_heads=heads) for l in range(distinct)]
+    bt, seq = lay[0]["block_table"], lay[0]["seq_lens"]
+    out = torch.empty((B, heads, 512), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((B, heads), dtype=torch.float32, device=device)
+    ws = mla.make_workspace(B, heads, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    sh = stream.cuda_stream
+
+    def step():
+        mla.mla_decode_plan(seq, bt, w.block_size, ws, num_heads=heads, dev_status=status,
+                            stream=sh, num_blocks=w.num_blocks())
+        for l in range(layers):
+            d = lay[l % distinct]
+            mla.mla_decode_planned(d["q"], d["cache"], bt, seq, mi.SOFTMAX_SCALE, out, lse,
+                                   workspace=ws, dev_status=status, stream=sh)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    cache_bytes = B * L_tok * mi.ROW * 2 * layers
+    return {"what": "one TP=8 rank: the node batch of 159 x 4096 sequences, 16 heads "
+                    "(padded to the kernel's 128), decoded over every layer's full cache",
+            "heads": heads, "batch": B, "layers": layers, "ms_per_step": round(ms, 3),
+            "cache_gb_per_step": round(cache_bytes / 1e9, 3),
+            "cache_gbs": round(cache_bytes / (ms * 1e-3) / 1e9, 1),
+            "frac_of_hbm_peak": round(cache_bytes / (ms * 1e-3) / 1e9 / hbm_peak, 4),
+            "vs_dp_rank_step": round(ms / dp_ms_step, 2),
+            "caches": f"{distinct} distinct layer caches of {B * L_tok * mi.ROW * 2 / 1e9:.2f} GB, "
+                      f"cycled"}
 
 
 # ----------------------------------------------------------------------------- oracle on the host
@@ -566,6 +627,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-absorption", action="store_true",
                     help="skip the separate timing of the absorption GEMMs")
+    ap.add_argument("--tp-compare", action="store_true",
+                    help="also time one TP=8 rank's step over the same node batch (16 heads)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--layers", type=int, default=0,
                     help="run only the first N layers of the workload (for profiling captures)")

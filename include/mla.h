@@ -149,7 +149,12 @@ mla_status_t mla_decode_plan(const int32_t *seq_lens, const int32_t *block_table
  *                 do not matter (the plan rewrites everything the decode
  *                 reads).  Calls sharing one workspace must not overlap on
  *                 the GPU.
- * Requirements: num_heads == 128; block_size in {16, 32, 64, 128, 256};
+ * Requirements: 1 <= num_heads <= 128 (mla_decode and mla_decode_planned;
+ * below 128 — a tensor-parallel rank's share of the heads, e.g. 16 at TP = 8
+ * [dp-attention-expert-parallel-mla-kv-replication (inferenceinterviews.com),
+ * "A strong answer"] — q is padded to 128 heads inside the workspace, which
+ * mla_decode_workspace_size(batch, num_heads) sizes for it; the other decode
+ * entry points need 128); block_size in {16, 32, 64, 128, 256};
  * max_seq_len <= max_blocks_per_seq * block_size <= 2^30; batch *
  * ceil(max_blocks_per_seq * block_size / 64) < 2^31 (the plan counts 64-token
  * units in int32); batch >= 0 (0 = no-op).  Else MLA_ERR_INVALID_ARGUMENT.

@@ -69,6 +69,31 @@ int sm_count_current(int *out_dev) {
 // Ranges of the plan: one per co-resident CTA pair of the tensor-core kernel.
 int max_ranges_current() { return tc_max_pairs(); }
 
+// Fewer heads than the kernel's 128 (a tensor-parallel rank's share): the
+// workspace holds q padded to 128 heads and the padded output and lse, behind
+// the plan and partials.  The pad heads hold whatever the workspace held:
+// every head is an independent row of the kernel's work and of the merge, and
+// only the caller's heads are copied out.
+struct Padded {
+  size_t q, out, lse, total;
+};
+Padded padded_layout(int32_t batch) {
+  Padded p;
+  p.q = 0;
+  p.out = align256(p.q + (size_t)batch * kHeads * kRow * 2);
+  p.lse = align256(p.out + (size_t)batch * kHeads * kVDim * 2);
+  p.total = align256(p.lse + (size_t)batch * kHeads * 4);
+  return p;
+}
+
+// mla_decode_partial / mla_combine_planned / mla_decode_append_planned work on
+// the kernel's own 128 heads only
+mla_status_t need_all_heads(int32_t num_heads) {
+  if (num_heads != kHeads)
+    return fail(MLA_ERR_UNSUPPORTED, "num_heads %d: this entry point needs %d", num_heads, kHeads);
+  return MLA_OK;
+}
+
 bool block_size_ok(int32_t bs) { return bs == 16 || bs == 32 || bs == 64 || bs == 128 || bs == 256; }
 
 mla_status_t check_decode_args(const void *q, const void *cache, int64_t num_blocks,
@@ -77,8 +102,8 @@ mla_status_t check_decode_args(const void *q, const void *cache, int64_t num_blo
                                int32_t num_heads, int32_t max_seq_len, float softmax_scale,
                                void *out, float *lse, void *workspace, size_t workspace_bytes) {
   if (batch < 0) return fail(MLA_ERR_INVALID_ARGUMENT, "batch %d < 0", batch);
-  if (num_heads != kHeads)
-    return fail(MLA_ERR_UNSUPPORTED, "num_heads %d: only %d is supported", num_heads, kHeads);
+  if (num_heads < 1 || num_heads > kHeads)
+    return fail(MLA_ERR_UNSUPPORTED, "num_heads %d: 1 to %d are supported", num_heads, kHeads);
   if (block_size <= 0) return fail(MLA_ERR_INVALID_ARGUMENT, "block_size %d <= 0", block_size);
   if (!block_size_ok(block_size))
     return fail(MLA_ERR_UNSUPPORTED, "block_size %d not in {16,32,64,128,256}", block_size);
@@ -160,10 +185,11 @@ mla_status_t mla_cache_append(const void *kv_new, const int64_t *slot_mapping, i
 }
 
 size_t mla_decode_workspace_size(int32_t batch, int32_t num_heads) {
-  if (batch < 0 || num_heads <= 0) return 0;
+  if (batch < 0 || num_heads <= 0 || num_heads > kHeads) return 0;
   const int ranges = max_ranges_current();
   if (ranges <= 0) return 0;
-  return workspace_layout(batch, num_heads, ranges).total;
+  const size_t plan = workspace_layout(batch, kHeads, ranges).total;
+  return num_heads == kHeads ? plan : plan + padded_layout(batch).total;
 }
 
 mla_status_t mla_decode_plan(const int32_t *seq_lens, const int32_t *block_table, int32_t batch,
@@ -172,7 +198,8 @@ mla_status_t mla_decode_plan(const int32_t *seq_lens, const int32_t *block_table
                              int32_t *dev_status, void *stream) {
   g_detail.clear();
   if (batch < 0) return fail(MLA_ERR_INVALID_ARGUMENT, "batch < 0");
-  if (num_heads != kHeads) return fail(MLA_ERR_UNSUPPORTED, "num_heads must be %d", kHeads);
+  if (num_heads < 1 || num_heads > kHeads)
+    return fail(MLA_ERR_UNSUPPORTED, "num_heads %d: 1 to %d are supported", num_heads, kHeads);
   if (!block_size_ok(block_size)) return fail(MLA_ERR_UNSUPPORTED, "block_size %d", block_size);
   if (batch == 0) return MLA_OK;
   if (!seq_lens || !workspace) return fail(MLA_ERR_INVALID_ARGUMENT, "null pointer");
@@ -188,7 +215,7 @@ mla_status_t mla_decode_plan(const int32_t *seq_lens, const int32_t *block_table
     return fail(MLA_ERR_INVALID_ARGUMENT, "num_blocks must be > 0 with a block table");
   cudaError_t e = launch_plan(seq_lens, block_table, num_blocks, batch, tc_unit_tokens(),
                               max_blocks_per_seq, block_size, max_ranges_current(), workspace,
-                              num_heads, dev_status, (cudaStream_t)stream);
+                              kHeads, dev_status, (cudaStream_t)stream);
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "plan launch");
 }
 
@@ -200,6 +227,7 @@ mla_status_t mla_decode_partial(const void *q, void *cache, const void *kv_new,
                                 void *workspace, size_t workspace_bytes, int32_t *dev_status,
                                 void *stream) {
   g_detail.clear();
+  if (need_all_heads(num_heads) != MLA_OK) return MLA_ERR_UNSUPPORTED;
   mla_status_t s = check_decode_args(q, cache, num_blocks, block_size, block_table,
                                      max_blocks_per_seq, seq_lens, batch, num_heads, max_seq_len,
                                      softmax_scale, out, lse, workspace, workspace_bytes);
@@ -255,6 +283,36 @@ mla_status_t mla_decode_planned(const void *q, const void *cache, int64_t num_bl
                                 int32_t batch, int32_t num_heads, int32_t max_seq_len,
                                 float softmax_scale, void *out, float *lse, void *workspace,
                                 size_t workspace_bytes, int32_t *dev_status, void *stream) {
+  if (num_heads != kHeads) {  // a tensor-parallel rank's heads, padded to 128
+    g_detail.clear();
+    mla_status_t st = check_decode_args(q, cache, num_blocks, block_size, block_table,
+                                        max_blocks_per_seq, seq_lens, batch, num_heads,
+                                        max_seq_len, softmax_scale, out, lse, workspace,
+                                        workspace_bytes);
+    if (st != MLA_OK || batch == 0) return st;
+    const Padded pl = padded_layout(batch);
+    char *pad = (char *)workspace + workspace_layout(batch, kHeads, max_ranges_current()).total;
+    void *q_pad = pad + pl.q, *out_pad = pad + pl.out;
+    float *lse_pad = (float *)(pad + pl.lse);
+    const size_t qrow = (size_t)num_heads * kRow * 2, orow = (size_t)num_heads * kVDim * 2;
+    cudaError_t e = cudaMemcpy2DAsync(q_pad, (size_t)kHeads * kRow * 2, q, qrow, qrow, batch,
+                                      cudaMemcpyDeviceToDevice, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "q copy into the padded heads");
+    st = mla_decode_partial(q_pad, const_cast<void *>(cache), nullptr, num_blocks, block_size,
+                            block_table, max_blocks_per_seq, seq_lens, batch, kHeads, max_seq_len,
+                            softmax_scale, out_pad, lse_pad, workspace, workspace_bytes,
+                            dev_status, stream);
+    if (st != MLA_OK) return st;
+    st = mla_combine_planned(workspace, workspace_bytes, batch, kHeads, out_pad, lse_pad, stream);
+    if (st != MLA_OK) return st;
+    e = cudaMemcpy2DAsync(out, orow, out_pad, (size_t)kHeads * kVDim * 2, orow, batch,
+                          cudaMemcpyDeviceToDevice, (cudaStream_t)stream);
+    if (e == cudaSuccess && lse)
+      e = cudaMemcpy2DAsync(lse, (size_t)num_heads * 4, lse_pad, (size_t)kHeads * 4,
+                            (size_t)num_heads * 4, batch, cudaMemcpyDeviceToDevice,
+                            (cudaStream_t)stream);
+    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "output copy from the padded heads");
+  }
   mla_status_t s = mla_decode_partial(q, const_cast<void *>(cache), nullptr, num_blocks,
                                       block_size, block_table, max_blocks_per_seq, seq_lens,
                                       batch, num_heads, max_seq_len, softmax_scale, out, lse,

@@ -59,8 +59,11 @@ def test_host_validation_before_any_launch(lib):
     args = lambda batch, heads, bs: (None, None, 1, bs, None, 1, None, batch, heads, 1, 0.1,
                                      None, None, None, 0, None, None)
     assert lib.mla_decode(*args(-1, 128, 64)) == 1
-    assert lib.mla_decode(*args(2, 64, 64)) == 2          # heads other than 128
+    assert lib.mla_decode(*args(2, 129, 64)) == 2         # more heads than 128
     assert b"num_heads" in lib.mla_last_error_detail()
+    assert lib.mla_decode(*args(2, 0, 64)) == 2
+    assert lib.mla_decode(*args(2, 16, 64)) == 1          # a TP rank's 16 heads: past the
+                                                          # head check, then null pointers
     assert lib.mla_decode(*args(2, 128, 48)) == 2         # unsupported page size
     assert lib.mla_decode(*args(2, 128, 0)) == 1
     assert lib.mla_decode(*args(0, 128, 64)) == 0         # empty batch: valid no-op
@@ -88,3 +91,19 @@ def test_absorption_host_validation(lib):
     assert lib.mla_absorb_out(None, None, 0, 128, None, None) == 0
     assert lib.mla_absorb_out(None, None, 4, 128, None, None) == 1
     assert lib.mla_absorb_out(None, None, 4, 100, None, None) == 2
+
+
+def test_partial_entry_points_need_all_heads(lib):
+    P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    lib.mla_decode_partial.argtypes = [P, P, P, i64, i32, P, i32, P, i32, i32, i32, f32, P, P, P,
+                                       sz, P, P]
+    lib.mla_decode_partial.restype = ctypes.c_int
+    lib.mla_combine_planned.argtypes = [P, sz, i32, i32, P, P, P]
+    lib.mla_combine_planned.restype = ctypes.c_int
+    # the split form works on the kernel's 128 heads; fewer go through mla_decode(_planned)
+    assert lib.mla_decode_partial(None, None, None, 1, 64, None, 1, None, 2, 16, 1, 0.1, None,
+                                  None, None, 0, None, None) == 2
+    assert lib.mla_combine_planned(None, 0, 2, 16, None, None, None) == 2
+    lib.mla_decode_workspace_size.argtypes = [i32, i32]
+    lib.mla_decode_workspace_size.restype = sz
+    assert lib.mla_decode_workspace_size(4, 129) == 0

@@ -777,3 +777,35 @@ def test_absorbed_layer_chain_matches_oracle(mla):
     out_ref, _ = oracle.decode(q_ref_bits, host_bits(dl["cache"]), dl["block_table_host"],
                                np.array(lens, np.int32), dl["softmax_scale"])
     assert_close(host_f64(o), oracle.absorb_out(out_ref, x["w_uv"]), "absorbed layer")
+
+
+# ------------------------------------------------------------ fewer heads (a TP rank)
+
+@pytest.mark.parametrize("heads", [1, 16, 64])
+@pytest.mark.parametrize("planned", [False, True])
+def test_fewer_heads_against_oracle(mla, heads, planned):
+    """A tensor-parallel rank's share of the heads (16 at TP = 8) over the same
+    cache: the library pads q to 128 heads in its workspace; only the caller's
+    heads come back, and they match the oracle."""
+    lens = [1, 17, 64, 200, 1500]
+    w = mi.custom_workload(lens, block_size=64, append=False, pool_factor=1.5)
+    dl = mi.make_device_layer(w, 0, "cuda", q_kind="sharp", num_heads=heads)
+    B = len(lens)
+    out = torch.full((B, heads, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, heads), float("nan"), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = mla.make_workspace(B, heads)
+    if planned:
+        mla.mla_decode_plan(dl["seq_lens"], dl["block_table"], w.block_size, ws, num_heads=heads,
+                            dev_status=status)
+        mla.mla_decode_planned(dl["q"], dl["cache"], dl["block_table"], dl["seq_lens"],
+                               dl["softmax_scale"], out, lse, workspace=ws, dev_status=status)
+    else:
+        mla.mla_decode(dl["q"], dl["cache"], dl["block_table"], dl["seq_lens"],
+                       dl["softmax_scale"], out, lse, workspace=ws, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref, ref_lse = oracle.decode(host_bits(dl["q"]), host_bits(dl["cache"]), dl["block_table_host"],
+                                 np.array(lens, np.int32), dl["softmax_scale"])
+    assert_close(host_f64(out), ref, f"{heads} heads")
+    assert_lse_close(lse.cpu().numpy(), ref_lse)
