@@ -301,8 +301,15 @@ def run_mine(args, w, rank, world, local_rank):
 
     # Dependencies between the copy streams and the compute stream are set
     # per chunk of layers rather than per layer (fewer cross-stream edges in
-    # the graph; each adds scheduling latency in front of a kernel).
+    # the graph; each adds scheduling latency in front of a kernel).  The
+    # first and last chunks are one layer: the first chunk's inputs and the
+    # last chunk's outputs cannot overlap any decode of the step.
     chunk = 3
+    if L >= 3:
+        bounds = [0, 1] + list(range(1 + chunk, L - 1, chunk)) + [L - 1, L]
+    else:
+        bounds = list(range(L + 1))
+    chunks = [(a, b) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
 
     def e2e_step():
         hs.wait_stream(stream)
@@ -310,20 +317,20 @@ def run_mine(args, w, rank, world, local_rank):
             seqd.copy_(seq_host, non_blocking=True)
             btd.copy_(bt_host, non_blocking=True)
             ev_in = []
-            for c0 in range(0, L, chunk):
-                for l in range(c0, min(L, c0 + chunk)):
+            for c0, c1 in chunks:
+                for l in range(c0, c1):
                     qd[l].copy_(q_host[l], non_blocking=True)
                     kvd[l].copy_(kv_host[l], non_blocking=True)
                 e = torch.cuda.Event()
                 e.record(hs)
                 ev_in.append(e)
         ds.wait_stream(stream)
-        for ci, c0 in enumerate(range(0, L, chunk)):
+        for ci, (c0, c1) in enumerate(chunks):
             stream.wait_event(ev_in[ci])
             if c0 == 0:
                 mla.mla_decode_plan(seqd, btd, w.block_size, ws, dev_status=status, stream=sh,
                                     num_blocks=w.num_blocks())
-            layers_c = range(c0, min(L, c0 + chunk))
+            layers_c = range(c0, c1)
             for l in layers_c:
                 d = W["layers"][l]
                 if w.append:
