@@ -424,7 +424,7 @@ def run_mine(args, w, rank, world, local_rank):
     }
     if not args.no_absorption:
         result["absorption"] = measure_absorption(w, device, stream, hbm_peak)
-    if args.tp_compare:
+    if not args.no_tp_compare and world == 1 and w.name.startswith("dp_rank"):
         result["tp_rank"] = measure_tp_rank(device, stream, hbm_peak, ms_step, L)
     if not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, W, budget_s=args.cpu_budget)
@@ -634,8 +634,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-absorption", action="store_true",
                     help="skip the separate timing of the absorption GEMMs")
-    ap.add_argument("--tp-compare", action="store_true",
-                    help="also time one TP=8 rank's step over the same node batch (16 heads)")
+    ap.add_argument("--no-tp-compare", action="store_true",
+                    help="skip timing one TP=8 rank's step over the same node batch (16 heads)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--layers", type=int, default=0,
                     help="run only the first N layers of the workload (for profiling captures)")
