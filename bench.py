@@ -270,6 +270,19 @@ def run_mine(args, w, rank, world, local_rank):
     ms_step = ms_total / args.steps
     assert int(status.item()) == 0, f"device status {int(status.item())}"
 
+    # ---- the same step uncaptured (eager launches), reported beside the graph's
+    eager_ms = None
+    if graph is not None:
+        k_eager = max(1, min(args.steps, 20))
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(k_eager):
+            step()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        eager_ms = reduce_max(g0.elapsed_time(g1) / k_eager, world, device)
+
     # ---- per-launch duration of the decode kernel (events around each launch)
     kev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
            for _ in range(L)]
@@ -405,6 +418,7 @@ def run_mine(args, w, rank, world, local_rank):
                    "cuda_graph": graph is not None,
                    "parallelism": "dp-attention rank per GPU; replicas only"},
         "step_roofline_frac": round(roofline_step_us / (ms_step * 1e3), 4),
+        "ms_per_step_uncaptured": round(eager_ms, 4) if eager_ms is not None else None,
         # all algorithmic bytes of the step (cache rows + q + out + appended
         # rows) per second, and against the nominal ~8 TB/s of GB300's HBM3e
         "algorithmic_gbs": round(world * step_bytes / (ms_step * 1e-3) / 1e9, 2),
