@@ -494,7 +494,7 @@ def measure_absorption(w, device, stream, hbm_peak, reps=20):
     per_layer = 2 * (128 * 128 * 512 * 2) + B * 128 * (128 + 64 + 576 + 512 + 128) * 2
     gbs = per_layer / (us_layer * 1e-6) / 1e9
     return {"what": "q = [q_nope . W_UK ; q_pe] and o = out . W_UV per layer (absorb_kernel, "
-                    "one launch each, in a CUDA graph), not part of the step's value",
+                    "one launch each, back to back in a CUDA graph), not part of the step's value",
             "us_per_layer": round(us_layer, 2), "us_per_step": round(us_layer * L, 1),
             "bytes_per_layer": per_layer, "achieved_gbs": round(gbs, 1),
             "frac_of_hbm_peak": round(gbs / hbm_peak, 4), "launches_per_layer": 2}

@@ -307,7 +307,11 @@ mla_status_t mla_decode_noalloc(const void *q, const void *cache, int64_t num_bl
  * All row-major and contiguous, 16-byte aligned; num_heads must be 128; any
  * B >= 0.  Each is one launch of a tensor-core kernel on `stream` (one CTA
  * per head and column tile streams the head's weight through TMA); nothing is
- * allocated and nothing is synchronised, so the calls can be captured.
+ * allocated and nothing is synchronised, so the calls can be captured.  The
+ * launch is a programmatic dependent of the previous kernel on the stream: it
+ * may start streaming the weight (which must not be written by that kernel)
+ * before that kernel ends; it reads the activations and writes its output
+ * only once that kernel has completed.
  *
  * Returns MLA_OK (B = 0: nothing enqueued), MLA_ERR_INVALID_ARGUMENT
  * (B < 0, null or misaligned pointers), MLA_ERR_UNSUPPORTED (num_heads), or

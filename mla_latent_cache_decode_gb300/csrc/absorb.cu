@@ -99,6 +99,26 @@ __global__ void __launch_bounds__(kThreads) absorb_kernel(const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
+  // Launched as a programmatic dependent: the next kernel may launch now, and
+  // this one's weight loads (constant across calls) may start before the
+  // previous kernel has finished.  Everything else — the activations it reads
+  // and every global write — comes after griddepcontrol.wait, which returns
+  // once the previous kernel has completed and its writes are visible.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  // the weight slabs of the first stages, ahead of the wait
+  if (warp == 0 && elect_one_sync()) {
+    prefetch_tmap(&maps.w);
+    for (int kc = 0; kc < nk && kc < ST; ++kc) {
+      const uint32_t bar = smem_u32(&s.full[kc]);
+      mbar_arrive_expect_tx(bar, (uint32_t)sbytes);
+      for (int j = 0; j < NT / 64; ++j)
+        tma_load_3d_hint(smem_u32(w_box(kc, j)), &maps.w, n0 + 64 * j, kc * kKChunk, h, bar,
+                         policy_evict_normal());
+    }
+  }
+  __syncwarp();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // the rotary dims of the query, copied behind the latent ones (one CTA per
   // head and row tile: the first column tile's)
@@ -116,18 +136,18 @@ __global__ void __launch_bounds__(kThreads) absorb_kernel(const __grid_constant_
   if (warp == 0) {
     if (elect_one_sync()) {  // TMA producer
       prefetch_tmap(&maps.a);
-      prefetch_tmap(&maps.w);
       for (int kc = 0; kc < nk; ++kc) {
         const int st = kc % ST;
-        const uint32_t par = ((kc / ST) & 1u) ^ 1u;
-        if (!mbar_wait(smem_u32(&s.empty[st]), par, nullptr, kWaitNs)) break;
         const uint32_t bar = smem_u32(&s.full[st]);
-        mbar_arrive_expect_tx(bar, (uint32_t)sbytes);
+        if (kc >= ST) {  // a later stage: its slot once free, then its weights too
+          if (!mbar_wait(smem_u32(&s.empty[st]), ((kc / ST) & 1u) ^ 1u, nullptr, kWaitNs)) break;
+          mbar_arrive_expect_tx(bar, (uint32_t)sbytes);
+          for (int j = 0; j < NT / 64; ++j)
+            tma_load_3d_hint(smem_u32(w_box(st, j)), &maps.w, n0 + 64 * j, kc * kKChunk, h, bar,
+                             policy_evict_normal());
+        }
         tma_load_3d_hint(smem_u32(a_box(st)), &maps.a, kc * kKChunk, h, m0, bar,
                          policy_evict_normal());
-        for (int j = 0; j < NT / 64; ++j)
-          tma_load_3d_hint(smem_u32(w_box(st, j)), &maps.w, n0 + 64 * j, kc * kKChunk, h, bar,
-                           policy_evict_normal());
       }
     }
     __syncwarp();
@@ -290,9 +310,17 @@ cudaError_t launch(const void *a, int k, const void *w, int n, int batch, void *
   p.ldc = ldc;
   p.c_head = c_head;
   p.rope = (const __nv_bfloat16 *)rope;
-  dim3 grid(n / NT, kHeads, (batch + 127) / 128);
-  absorb::absorb_kernel<NT, ST><<<grid, absorb::kThreads, smem, stream>>>(maps, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n / NT, kHeads, (batch + 127) / 128);
+  cfg.blockDim = dim3(absorb::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, absorb::absorb_kernel<NT, ST>, maps, p);
 }
 
 mla_status_t check(const void *const *ptrs, int count, int32_t batch, int32_t num_heads) {
