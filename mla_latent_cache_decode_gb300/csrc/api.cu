@@ -4,7 +4,6 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
-#include <mutex>
 #include <string>
 
 #include "common.cuh"
@@ -49,22 +48,6 @@ mla_status_t cuda_fail(cudaError_t e, const char *what) {
 }
 
 bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
-
-// Per-device SM count, cached (the only host state besides g_detail).
-int sm_count_current(int *out_dev) {
-  static std::mutex mu;
-  static int counts[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
-  if (out_dev) *out_dev = dev;
-  std::lock_guard<std::mutex> lock(mu);
-  if (counts[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-    counts[dev] = n;
-  }
-  return counts[dev];
-}
 
 // Ranges of the plan: one per co-resident CTA pair of the tensor-core kernel.
 int max_ranges_current() { return tc_max_pairs(); }
