@@ -371,6 +371,23 @@ mla_status_t mla_place_requests(const int64_t *kv_tokens, int32_t n, int32_t ran
 mla_status_t mla_place_one(const int64_t *rank_load, int32_t ranks, int64_t capacity_tokens,
                            int64_t kv_tokens, int32_t *rank);
 
+/*
+ * mla_selftest_wait_timeout — checks, on the device, the bounded waits every
+ * kernel of this library uses, without a fault or a hang.  One block of two
+ * warps: warp 0 waits on an mbarrier that nothing arrives at, with a budget
+ * of budget_ns; when it gives up it raises the block's abort flag and
+ * reports MLA_ERR_DEVICE_TIMEOUT into *dev_status (first error wins).  Warp 1
+ * waits on another such barrier through the decode kernel's own wait (100 ms
+ * budget, ended early by the abort flag).  elapsed_ns[0..1] (device, uint64)
+ * receive each warp's wait time in ns (0 if its wait completed).  The kernel
+ * returns normally; the context stays usable.  Asynchronous on `stream`.
+ *
+ * Returns MLA_OK, MLA_ERR_INVALID_ARGUMENT (budget_ns outside 1 us .. 1 s,
+ * a null or misaligned pointer) or MLA_ERR_CUDA (launch failure).
+ */
+mla_status_t mla_selftest_wait_timeout(uint64_t budget_ns, int32_t *dev_status,
+                                       uint64_t *elapsed_ns, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -30,7 +30,7 @@ EXPORTED = ("mla_status_string", "mla_last_error_detail", "mla_abi_version", "ml
             "mla_decode_workspace_size", "mla_decode_plan", "mla_decode", "mla_decode_planned",
             "mla_combine", "mla_decode_noalloc", "mla_decode_partial", "mla_combine_planned",
             "mla_decode_append_planned", "mla_place_requests", "mla_place_one", "mla_absorb_q",
-            "mla_absorb_out")
+            "mla_absorb_out", "mla_selftest_wait_timeout")
 
 
 class MlaError(RuntimeError):
@@ -84,6 +84,8 @@ def _load():
     lib.mla_absorb_q.restype = ctypes.c_int
     lib.mla_absorb_out.argtypes = [P, P, i32, i32, P, P]
     lib.mla_absorb_out.restype = ctypes.c_int
+    lib.mla_selftest_wait_timeout.argtypes = [ctypes.c_uint64, P, P, P]
+    lib.mla_selftest_wait_timeout.restype = ctypes.c_int
     return lib
 
 
@@ -362,3 +364,16 @@ def mla_absorb_out(out, w_uv, o, stream=None):
         raise ValueError("shapes: out [B,H,512], w_uv [H,512,128], o [B,H,128]")
     _check(get_lib().mla_absorb_out(_ptr(out), _ptr(w_uv), B, H, _ptr(o), _stream(stream)))
     return o
+
+
+def selftest_wait_timeout(budget_ns: int, dev_status, elapsed_ns, stream=None):
+    """Runs the device check of the bounded waits (mla_selftest_wait_timeout):
+    dev_status int32 [1] receives MLA_ERR_DEVICE_TIMEOUT, elapsed_ns int64 [2]
+    each warp's wait time in ns.  Asynchronous on `stream`."""
+    import torch
+    _need(dev_status, torch.int32, 1, "dev_status")
+    _need(elapsed_ns, torch.int64, 1, "elapsed_ns")
+    if elapsed_ns.shape[0] < 2:
+        raise ValueError("elapsed_ns needs 2 entries")
+    _check(get_lib().mla_selftest_wait_timeout(int(budget_ns), _ptr(dev_status), _ptr(elapsed_ns),
+                                               _stream(stream)))

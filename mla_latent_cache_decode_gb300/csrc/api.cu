@@ -21,6 +21,8 @@ cudaError_t launch_plan_combine(void *ws, int32_t batch, int32_t heads, int32_t 
 cudaError_t launch_offsets_combine(const float *o_part, const float *lse_part,
                                    const int32_t *offsets, int32_t batch, int32_t heads, void *out,
                                    float *lse, cudaStream_t stream);
+cudaError_t launch_wait_selftest(int32_t *dev_status, uint64_t budget_ns, uint64_t *elapsed_ns,
+                                 cudaStream_t stream);
 int tc_unit_tokens();
 int tc_max_pairs();
 cudaError_t launch_decode_tc(const void *q, const void *cache, int64_t num_blocks, int32_t block_size,
@@ -338,6 +340,19 @@ mla_status_t mla_combine(const float *o_partial, const float *lse_partial,
   cudaError_t e = launch_offsets_combine(o_partial, lse_partial, split_offsets, batch, num_heads,
                                          out, lse, (cudaStream_t)stream);
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "combine launch");
+}
+
+mla_status_t mla_selftest_wait_timeout(uint64_t budget_ns, int32_t *dev_status,
+                                       uint64_t *elapsed_ns, void *stream) {
+  g_detail.clear();
+  if (budget_ns < 1000 || budget_ns > 1000000000ull)
+    return fail(MLA_ERR_INVALID_ARGUMENT, "budget_ns %llu: 1 us to 1 s",
+                (unsigned long long)budget_ns);
+  if (!dev_status || !elapsed_ns) return fail(MLA_ERR_INVALID_ARGUMENT, "null pointer");
+  if (!aligned(dev_status, 4) || !aligned(elapsed_ns, 8))
+    return fail(MLA_ERR_INVALID_ARGUMENT, "dev_status / elapsed_ns alignment");
+  cudaError_t e = launch_wait_selftest(dev_status, budget_ns, elapsed_ns, (cudaStream_t)stream);
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e, "self-test launch");
 }
 
 }  // extern "C"

@@ -835,7 +835,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Check of the bounded waits, without a fault or a hang: warp 0 waits on a
+// barrier nothing arrives at, with budget_ns; when its wait gives up it raises
+// the abort flag and reports MLA_ERR_DEVICE_TIMEOUT, as the decode's roles do.
+// Warp 1 waits on another such barrier through the decode's own warp_wait
+// (100 ms budget, released by the abort flag), so it returns soon after warp
+// 0 gives up.  Each warp's wait time goes to elapsed_ns[warp]; the kernel
+// then ends normally and the context stays usable.
+__global__ void __launch_bounds__(64) wait_selftest_kernel(int32_t *dev_status, uint64_t budget_ns,
+                                                           uint64_t *elapsed_ns) {
+  __shared__ __align__(8) uint64_t bar[2];
+  __shared__ int abort;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar[0]), 1);
+    mbar_init(smem_u32(&bar[1]), 1);
+    abort = 0;
+    fence_mbarrier_init_cluster();
+  }
+  __syncthreads();
+  volatile int *abort_flag = &abort;
+  const uint64_t t0 = globaltimer();
+  bool ok;
+  if (warp == 0) {
+    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar[0]), 0, nullptr, budget_ns));
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      report(dev_status, MLA_ERR_DEVICE_TIMEOUT);
+    }
+  } else {
+    ok = warp_wait(smem_u32(&bar[1]), 0, abort_flag);
+  }
+  if (lane == 0) elapsed_ns[warp] = ok ? 0 : globaltimer() - t0;
+}
+
 }  // namespace tc
+
+cudaError_t launch_wait_selftest(int32_t *dev_status, uint64_t budget_ns, uint64_t *elapsed_ns,
+                                 cudaStream_t stream) {
+  tc::wait_selftest_kernel<<<1, 64, 0, stream>>>(dev_status, budget_ns, elapsed_ns);
+  return cudaGetLastError();
+}
 
 // ---------------------------------------------------------------------------- host
 

@@ -75,6 +75,22 @@ def test_host_validation_before_any_launch(lib):
     assert lib.mla_combine(None, None, None, 2, 128, None, None, None) == 1
 
 
+def test_wait_selftest_host_validation(lib):
+    P = ctypes.c_void_p
+    lib.mla_selftest_wait_timeout.argtypes = [ctypes.c_uint64, P, P, P]
+    lib.mla_selftest_wait_timeout.restype = ctypes.c_int
+    lib.mla_last_error_detail.restype = ctypes.c_char_p
+    st, el = ctypes.c_int32(0), (ctypes.c_uint64 * 2)()
+    pst, pel = ctypes.addressof(st), ctypes.addressof(el)
+    assert lib.mla_selftest_wait_timeout(0, pst, pel, None) == 1           # budget below 1 us
+    assert b"budget_ns" in lib.mla_last_error_detail()
+    assert lib.mla_selftest_wait_timeout(2_000_000_000, pst, pel, None) == 1  # above 1 s
+    assert lib.mla_selftest_wait_timeout(1_000_000, None, pel, None) == 1
+    assert lib.mla_selftest_wait_timeout(1_000_000, pst, None, None) == 1
+    assert lib.mla_selftest_wait_timeout(1_000_000, pst + 1, pel, None) == 1  # misaligned
+    assert st.value == 0  # nothing launched
+
+
 def test_absorption_host_validation(lib):
     P, i32 = ctypes.c_void_p, ctypes.c_int32
     lib.mla_absorb_q.argtypes = [P, P, P, i32, i32, P, P]

@@ -252,6 +252,29 @@ def test_seq_len_longer_than_table_is_flagged(mla):
     assert st == 5
 
 
+@pytest.mark.parametrize("budget_ms", [1, 5])
+def test_bounded_wait_times_out_and_context_survives(mla, budget_ms):
+    # a wait on a barrier nothing arrives at gives up after its budget and
+    # reports MLA_ERR_DEVICE_TIMEOUT; the other warp's wait (the decode's own,
+    # 100 ms budget) is ended by the abort flag well before its budget; the
+    # kernel returns and the context stays usable
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    elapsed = torch.zeros(2, dtype=torch.int64, device="cuda")
+    mla.selftest_wait_timeout(budget_ms * 1_000_000, status, elapsed)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 6
+    e0, e1 = (int(x) for x in elapsed.cpu())
+    assert budget_ms * 1_000_000 <= e0 < 90_000_000, e0
+    assert budget_ms * 1_000_000 <= e1 < 90_000_000, e1  # under its own 100 ms
+    w = mi.workload(1)
+    d = mi.make_host_layer(w, mi.rng_for(1))
+    cache, out, lse, st = run_layer(mla, d)
+    assert st == 0
+    ref_cache, ref, ref_lse = oracle_layer(d)
+    assert np.array_equal(host_bits(cache), ref_cache)
+    assert_close(host_f64(out), ref, "decode after the timeout check")
+
+
 def test_host_validation_errors(mla):
     q = torch.zeros((1, 128, 576), dtype=torch.bfloat16, device="cuda")
     cache = torch.zeros((4, 16, 576), dtype=torch.bfloat16, device="cuda")
