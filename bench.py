@@ -153,20 +153,24 @@ def algorithmic_bytes_per_layer(w):
 KERNEL_SOURCES = ("mla_latent_cache_decode_gb300/csrc/decode_tc.cu",
                   "mla_latent_cache_decode_gb300/csrc/sm100.cuh",
                   "mla_latent_cache_decode_gb300/csrc/common.cuh")
-KERNEL_HEADER = "include/mla.h"  # only its #define MLA_ constants reach the kernel
+KERNEL_HEADER = "include/mla.h"
+# the header's constants that reach the decode kernel (its declarations,
+# comments, ABI version and the no-allocation entry point's limits do not)
+KERNEL_CONSTANTS = ("MLA_ROW_DIM", "MLA_KV_LORA_RANK", "MLA_ROPE_DIM", "MLA_NUM_HEADS")
 TRAFFIC_PROFILE = "profiles/decode_tc_dp_rank_layer_b20x4096_dram.md"
 
 
 def kernel_source_hash():
-    """sha256 of the decode kernel's sources and of the header's MLA_ constants
-    (the header's declarations and comments do not change the kernel)."""
+    """sha256 of the decode kernel's sources and of the header constants that
+    reach it."""
     import hashlib
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     with open(os.path.join(ROOT, KERNEL_HEADER)) as fh:
-        consts = [ln.strip() for ln in fh if ln.startswith("#define MLA_")]
+        consts = [ln.strip() for ln in fh
+                  if ln.startswith("#define ") and ln.split()[1] in KERNEL_CONSTANTS]
     h.update("\n".join(consts).encode())
     return h.hexdigest()
 

@@ -57,7 +57,7 @@
 extern "C" {
 #endif
 
-#define MLA_ABI_VERSION 2
+#define MLA_ABI_VERSION 3
 #define MLA_ROW_DIM 576       /* 512 kv_c + 64 k_rope per cached token */
 #define MLA_KV_LORA_RANK 512  /* value / output width */
 #define MLA_ROPE_DIM 64
@@ -313,14 +313,19 @@ mla_status_t mla_decode_noalloc(const void *q, const void *cache, int64_t num_bl
  * before that kernel ends; it reads the activations and writes its output
  * only once that kernel has completed.
  *
+ * dev_status (device int32, nullable) receives MLA_ERR_DEVICE_TIMEOUT (first
+ * error wins) if one of the kernel's bounded waits runs out (100 ms each); the
+ * block then stores nothing, waits (bounded) for its issued copies and MMAs
+ * and returns, and the output is undefined.
+ *
  * Returns MLA_OK (B = 0: nothing enqueued), MLA_ERR_INVALID_ARGUMENT
  * (B < 0, null or misaligned pointers), MLA_ERR_UNSUPPORTED (num_heads), or
  * MLA_ERR_CUDA.
  */
 mla_status_t mla_absorb_q(const void *q_nope, const void *q_pe, const void *w_uk, int32_t batch,
-                          int32_t num_heads, void *q, void *stream);
+                          int32_t num_heads, void *q, int32_t *dev_status, void *stream);
 mla_status_t mla_absorb_out(const void *out, const void *w_uv, int32_t batch, int32_t num_heads,
-                            void *o, void *stream);
+                            void *o, int32_t *dev_status, void *stream);
 
 /*
  * mla_place_requests — KV-load-aware placement of requests on data-parallel

@@ -80,9 +80,9 @@ def _load():
     lib.mla_place_requests.restype = ctypes.c_int
     lib.mla_place_one.argtypes = [P, i32, i64, i64, P]
     lib.mla_place_one.restype = ctypes.c_int
-    lib.mla_absorb_q.argtypes = [P, P, P, i32, i32, P, P]
+    lib.mla_absorb_q.argtypes = [P, P, P, i32, i32, P, P, P]
     lib.mla_absorb_q.restype = ctypes.c_int
-    lib.mla_absorb_out.argtypes = [P, P, i32, i32, P, P]
+    lib.mla_absorb_out.argtypes = [P, P, i32, i32, P, P, P]
     lib.mla_absorb_out.restype = ctypes.c_int
     lib.mla_selftest_wait_timeout.argtypes = [ctypes.c_uint64, P, P, P]
     lib.mla_selftest_wait_timeout.restype = ctypes.c_int
@@ -336,8 +336,9 @@ def place_one(rank_load, kv_tokens: int, capacity_tokens: int = 0) -> int:
     return rank.value
 
 
-def mla_absorb_q(q_nope, q_pe, w_uk, q, stream=None):
-    """q[b,h,0:512] = q_nope[b,h] . W_UK[h]; q[b,h,512:576] = q_pe[b,h] (mla_absorb_q)."""
+def mla_absorb_q(q_nope, q_pe, w_uk, q, dev_status=None, stream=None):
+    """q[b,h,0:512] = q_nope[b,h] . W_UK[h]; q[b,h,512:576] = q_pe[b,h] (mla_absorb_q).
+    dev_status: optional device int32 [1], set to MLA_ERR_DEVICE_TIMEOUT if a wait runs out."""
     import torch
     _need(q_nope, torch.bfloat16, 3, "q_nope")
     _need(q_pe, torch.bfloat16, 3, "q_pe")
@@ -348,12 +349,12 @@ def mla_absorb_q(q_nope, q_pe, w_uk, q, stream=None):
             or tuple(w_uk.shape) != (H, 128, 512) or tuple(q.shape) != (B, H, ROW_DIM)):
         raise ValueError("shapes: q_nope [B,H,128], q_pe [B,H,64], w_uk [H,128,512], q [B,H,576]")
     _check(get_lib().mla_absorb_q(_ptr(q_nope), _ptr(q_pe), _ptr(w_uk), B, H, _ptr(q),
-                                  _stream(stream)))
+                                  _ptr(dev_status), _stream(stream)))
     return q
 
 
-def mla_absorb_out(out, w_uv, o, stream=None):
-    """o[b,h] = out[b,h] . W_UV[h] (mla_absorb_out)."""
+def mla_absorb_out(out, w_uv, o, dev_status=None, stream=None):
+    """o[b,h] = out[b,h] . W_UV[h] (mla_absorb_out).  dev_status as for mla_absorb_q."""
     import torch
     _need(out, torch.bfloat16, 3, "out")
     _need(w_uv, torch.bfloat16, 3, "w_uv")
@@ -362,7 +363,8 @@ def mla_absorb_out(out, w_uv, o, stream=None):
     if (tuple(out.shape) != (B, H, 512) or tuple(w_uv.shape) != (H, 512, 128)
             or tuple(o.shape) != (B, H, 128)):
         raise ValueError("shapes: out [B,H,512], w_uv [H,512,128], o [B,H,128]")
-    _check(get_lib().mla_absorb_out(_ptr(out), _ptr(w_uv), B, H, _ptr(o), _stream(stream)))
+    _check(get_lib().mla_absorb_out(_ptr(out), _ptr(w_uv), B, H, _ptr(o), _ptr(dev_status),
+                                    _stream(stream)))
     return o
 
 

@@ -38,6 +38,7 @@ constexpr int kNope = 128;                  // non-rotary query dims per head
 constexpr int kRope = 64;                   // shared rotary dims
 constexpr int kVHead = 128;                 // value dims per head after W_UV
 constexpr uint64_t kWaitNs = 100000000ull;  // 100 ms per wait
+constexpr uint64_t kDrainNs = 10000000ull;  // 10 ms to drain issued copies on abort
 
 // Dynamic shared memory, from a 1024-byte boundary: ST stages of
 // {W: NT / 64 boxes of kWBox, then A: a_rows x 128 B} (a_rows a multiple of 8,
@@ -58,6 +59,7 @@ struct Params {
   __nv_bfloat16 *c;            // C rows: c + b * ldc + h * c_head + n
   int64_t ldc, c_head;
   const __nv_bfloat16 *rope;   // absorb_q: q_pe [B][128][64], copied to c[..., 512:576]
+  int32_t *dev_status;         // nullable: MLA_ERR_DEVICE_TIMEOUT when a wait runs out
 };
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
@@ -73,6 +75,7 @@ __global__ void __launch_bounds__(kThreads) absorb_kernel(const __grid_constant_
   struct Bars {
     uint64_t full[ST], empty[ST], done;
     uint32_t tmem_base;
+    int abort;  // a wait ran out: the other roles stop waiting, nothing is stored
   };
   __shared__ Bars s;
   uint8_t *stages = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -88,6 +91,7 @@ __global__ void __launch_bounds__(kThreads) absorb_kernel(const __grid_constant_
       mbar_init(smem_u32(&s.empty[i]), 1);
     }
     mbar_init(smem_u32(&s.done), 1);
+    s.abort = 0;
     fence_mbarrier_init_cluster();
   }
   if (warp == 2) {
@@ -132,15 +136,24 @@ __global__ void __launch_bounds__(kThreads) absorb_kernel(const __grid_constant_
     }
   }
 
-  bool ok = true;
+  volatile int *abort_flag = &s.abort;
+  auto give_up = [&]() {
+    *abort_flag = 1;
+    report(prm.dev_status, MLA_ERR_DEVICE_TIMEOUT);
+  };
   if (warp == 0) {
     if (elect_one_sync()) {  // TMA producer
       prefetch_tmap(&maps.a);
+      // stages up to min(nk, ST) had their weights requested before the wait
+      int issued = 0;  // chunks whose loads are all issued
       for (int kc = 0; kc < nk; ++kc) {
         const int st = kc % ST;
         const uint32_t bar = smem_u32(&s.full[st]);
         if (kc >= ST) {  // a later stage: its slot once free, then its weights too
-          if (!mbar_wait(smem_u32(&s.empty[st]), ((kc / ST) & 1u) ^ 1u, nullptr, kWaitNs)) break;
+          if (!mbar_wait(smem_u32(&s.empty[st]), ((kc / ST) & 1u) ^ 1u, abort_flag, kWaitNs)) {
+            if (!*abort_flag) give_up();
+            break;
+          }
           mbar_arrive_expect_tx(bar, (uint32_t)sbytes);
           for (int j = 0; j < NT / 64; ++j)
             tma_load_3d_hint(smem_u32(w_box(st, j)), &maps.w, n0 + 64 * j, kc * kKChunk, h, bar,
@@ -148,6 +161,15 @@ __global__ void __launch_bounds__(kThreads) absorb_kernel(const __grid_constant_
         }
         tma_load_3d_hint(smem_u32(a_box(st)), &maps.a, kc * kKChunk, h, m0, bar,
                          policy_evict_normal());
+        issued = kc + 1;
+      }
+      if (*abort_flag) {
+        // no copy may still be landing when the shared memory is given up:
+        // wait (bounded) for the last chunk issued into each stage
+        for (int st = 0; st < ST && st < issued; ++st) {
+          const int last = st + ((issued - 1 - st) / ST) * ST;
+          (void)mbar_wait(smem_u32(&s.full[st]), (last / ST) & 1u, nullptr, kDrainNs);
+        }
       }
     }
     __syncwarp();
@@ -156,8 +178,8 @@ __global__ void __launch_bounds__(kThreads) absorb_kernel(const __grid_constant_
       const uint32_t id = idesc_bf16_f32(128, NT, 1);
       for (int kc = 0; kc < nk; ++kc) {
         const int st = kc % ST;
-        if (!mbar_wait(smem_u32(&s.full[st]), (kc / ST) & 1u, nullptr, kWaitNs)) {
-          ok = false;
+        if (!mbar_wait(smem_u32(&s.full[st]), (kc / ST) & 1u, abort_flag, kWaitNs)) {
+          if (!*abort_flag) give_up();
           break;
         }
         tc_fence_after();
@@ -169,14 +191,17 @@ __global__ void __launch_bounds__(kThreads) absorb_kernel(const __grid_constant_
                  (kc > 0 || kk > 0) ? 1u : 0u);
         mma_commit(smem_u32(&s.empty[st]));
       }
-      if (ok) mma_commit(smem_u32(&s.done));
+      // also after an abort: done then marks the completion of every MMA
+      // issued, so the tensor memory is freed only once they are finished
+      mma_commit(smem_u32(&s.done));
     }
     __syncwarp();
   }
 
   // epilogue: warp w holds rows m0 + 32w .. m0 + 32w + 31 in its TMEM lanes
   const bool done = mbar_wait(smem_u32(&s.done), 0, nullptr, kWaitNs);
-  if (__all_sync(0xffffffffu, done) && m0 + 32 * warp < prm.batch) {
+  if (!done && lane == 0) report(prm.dev_status, MLA_ERR_DEVICE_TIMEOUT);
+  if (__all_sync(0xffffffffu, done) && !*abort_flag && m0 + 32 * warp < prm.batch) {
     tc_fence_after();
     const int b = m0 + 32 * warp + lane;
     __nv_bfloat16 *row = prm.c + (int64_t)b * prm.ldc + h * prm.c_head + n0;
@@ -280,7 +305,7 @@ bool cached_encode(CUtensorMap *m, int dev, const void *base, uint64_t d0, uint6
 
 template <int NT, int ST>
 cudaError_t launch(const void *a, int k, const void *w, int n, int batch, void *c, int64_t ldc,
-                   int64_t c_head, const void *rope, cudaStream_t stream) {
+                   int64_t c_head, const void *rope, int32_t *dev_status, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -310,6 +335,7 @@ cudaError_t launch(const void *a, int k, const void *w, int n, int batch, void *
   p.ldc = ldc;
   p.c_head = c_head;
   p.rope = (const __nv_bfloat16 *)rope;
+  p.dev_status = dev_status;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n / NT, kHeads, (batch + 127) / 128);
   cfg.blockDim = dim3(absorb::kThreads);
@@ -360,7 +386,7 @@ using namespace mla;
 extern "C" {
 
 mla_status_t mla_absorb_q(const void *q_nope, const void *q_pe, const void *w_uk, int32_t batch,
-                          int32_t num_heads, void *q, void *stream) {
+                          int32_t num_heads, void *q, int32_t *dev_status, void *stream) {
   set_error_detail("");
   const void *ptrs[4] = {q_nope, q_pe, w_uk, q};
   mla_status_t s = check(ptrs, 4, batch, num_heads);
@@ -368,11 +394,11 @@ mla_status_t mla_absorb_q(const void *q_nope, const void *q_pe, const void *w_uk
   // q[b, h, 0:512] = q_nope[b, h, :] . W_UK[h]; q[b, h, 512:576] = q_pe[b, h, :]
   // 256 columns a CTA, the whole K (two chunks) in flight
   return launched(launch<256, 2>(q_nope, absorb::kNope, w_uk, kVDim, batch, q, (int64_t)kHeads * kRow,
-                              kRow, q_pe, (cudaStream_t)stream));
+                              kRow, q_pe, dev_status, (cudaStream_t)stream));
 }
 
 mla_status_t mla_absorb_out(const void *out, const void *w_uv, int32_t batch, int32_t num_heads,
-                            void *o, void *stream) {
+                            void *o, int32_t *dev_status, void *stream) {
   set_error_detail("");
   const void *ptrs[3] = {out, w_uv, o};
   mla_status_t s = check(ptrs, 3, batch, num_heads);
@@ -381,7 +407,7 @@ mla_status_t mla_absorb_out(const void *out, const void *w_uv, int32_t batch, in
   // 64 columns a CTA (two per head), the whole K (eight chunks) in flight
   return launched(launch<64, 8>(out, kVDim, w_uv, absorb::kVHead, batch, o,
                               (int64_t)kHeads * absorb::kVHead, absorb::kVHead, nullptr,
-                              (cudaStream_t)stream));
+                              dev_status, (cudaStream_t)stream));
 }
 
 }  // extern "C"

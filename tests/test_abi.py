@@ -41,7 +41,7 @@ def test_binding_names_match_header():
 def test_status_strings_and_version(lib):
     lib.mla_status_string.restype = ctypes.c_char_p
     lib.mla_abi_version.restype = ctypes.c_int
-    assert lib.mla_abi_version() == 2
+    assert lib.mla_abi_version() == 3
     names = [lib.mla_status_string(i).decode() for i in range(7)]
     assert names[0] == "MLA_OK" and names[6] == "MLA_ERR_DEVICE_TIMEOUT"
     assert lib.mla_status_string(99).decode() == "MLA_ERR_UNKNOWN"
@@ -93,20 +93,20 @@ def test_wait_selftest_host_validation(lib):
 
 def test_absorption_host_validation(lib):
     P, i32 = ctypes.c_void_p, ctypes.c_int32
-    lib.mla_absorb_q.argtypes = [P, P, P, i32, i32, P, P]
+    lib.mla_absorb_q.argtypes = [P, P, P, i32, i32, P, P, P]
     lib.mla_absorb_q.restype = ctypes.c_int
-    lib.mla_absorb_out.argtypes = [P, P, i32, i32, P, P]
+    lib.mla_absorb_out.argtypes = [P, P, i32, i32, P, P, P]
     lib.mla_absorb_out.restype = ctypes.c_int
     lib.mla_last_error_detail.restype = ctypes.c_char_p
-    assert lib.mla_absorb_q(None, None, None, 0, 128, None, None) == 0     # empty batch: no-op
-    assert lib.mla_absorb_q(None, None, None, -1, 128, None, None) == 1
-    assert lib.mla_absorb_q(None, None, None, 4, 64, None, None) == 2      # heads other than 128
-    assert lib.mla_absorb_q(None, None, None, 4, 128, None, None) == 1     # null pointers
+    assert lib.mla_absorb_q(None, None, None, 0, 128, None, None, None) == 0     # empty batch: no-op
+    assert lib.mla_absorb_q(None, None, None, -1, 128, None, None, None) == 1
+    assert lib.mla_absorb_q(None, None, None, 4, 64, None, None, None) == 2      # heads other than 128
+    assert lib.mla_absorb_q(None, None, None, 4, 128, None, None, None) == 1     # null pointers
     assert b"null" in lib.mla_last_error_detail()
-    assert lib.mla_absorb_q(16, 32, 48, 4, 128, 72, None) == 1             # misaligned
-    assert lib.mla_absorb_out(None, None, 0, 128, None, None) == 0
-    assert lib.mla_absorb_out(None, None, 4, 128, None, None) == 1
-    assert lib.mla_absorb_out(None, None, 4, 100, None, None) == 2
+    assert lib.mla_absorb_q(16, 32, 48, 4, 128, 72, None, None) == 1             # misaligned
+    assert lib.mla_absorb_out(None, None, 0, 128, None, None, None) == 0
+    assert lib.mla_absorb_out(None, None, 4, 128, None, None, None) == 1
+    assert lib.mla_absorb_out(None, None, 4, 100, None, None, None) == 2
 
 
 def test_partial_entry_points_need_all_heads(lib):
