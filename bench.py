@@ -477,12 +477,13 @@ def measure_absorption(w, device, stream, hbm_peak, reps=20):
     out = torch.randn((B, 128, 512), generator=g, device=device).to(bf)
     q = torch.empty((B, 128, mi.ROW), dtype=bf, device=device)
     o = torch.empty((B, 128, 128), dtype=bf, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
     sh = stream.cuda_stream
 
     def layers():
         for l in range(L):
-            mla.mla_absorb_q(q_nope, q_pe, w_uk[l], q, stream=sh)
-            mla.mla_absorb_out(out, w_uv[l], o, stream=sh)
+            mla.mla_absorb_q(q_nope, q_pe, w_uk[l], q, dev_status=status, stream=sh)
+            mla.mla_absorb_out(out, w_uv[l], o, dev_status=status, stream=sh)
 
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -500,6 +501,7 @@ def measure_absorption(w, device, stream, hbm_peak, reps=20):
         graph.replay()
     e1.record(stream)
     torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"absorption device status {int(status.item())}"
     us_layer = e0.elapsed_time(e1) * 1e3 / (reps * L)
     per_layer = 2 * (128 * 128 * 512 * 2) + B * 128 * (128 + 64 + 576 + 512 + 128) * 2
     gbs = per_layer / (us_layer * 1e-6) / 1e9
