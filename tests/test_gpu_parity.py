@@ -760,8 +760,11 @@ def test_absorb_q_matches_oracle(mla, B):
     out); q[b,h,512:] = q_pe[b,h] bit for bit."""
     x = _absorb_inputs(B, 100 + B)
     q = torch.empty((B, 128, 576), dtype=torch.bfloat16, device="cuda")
-    mla.mla_absorb_q(dev_bf16(x["q_nope"]), dev_bf16(x["q_pe"]), dev_bf16(x["w_uk"]), q)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.mla_absorb_q(dev_bf16(x["q_nope"]), dev_bf16(x["q_pe"]), dev_bf16(x["w_uk"]), q,
+                     dev_status=status)
     torch.cuda.synchronize()
+    assert int(status.item()) == 0
     ref = oracle.absorb_q(x["q_nope"], x["q_pe"], x["w_uk"])
     assert_close(host_f64(q)[:, :, :512], ref[:, :, :512], f"absorbed q B={B}")
     assert np.array_equal(host_bits(q)[:, :, 512:], x["q_pe"])
@@ -772,8 +775,10 @@ def test_absorb_out_matches_oracle(mla, B):
     """o[b,h] = out[b,h] . W_UV[h] within the parity bar."""
     x = _absorb_inputs(B, 200 + B)
     o = torch.empty((B, 128, 128), dtype=torch.bfloat16, device="cuda")
-    mla.mla_absorb_out(dev_bf16(x["out"]), dev_bf16(x["w_uv"]), o)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.mla_absorb_out(dev_bf16(x["out"]), dev_bf16(x["w_uv"]), o, dev_status=status)
     torch.cuda.synchronize()
+    assert int(status.item()) == 0
     assert_close(host_f64(o), oracle.absorb_out(x["out"], x["w_uv"]), f"absorbed out B={B}")
 
 
@@ -789,10 +794,11 @@ def test_absorbed_layer_chain_matches_oracle(mla):
     out = torch.empty((B, 128, 512), dtype=torch.bfloat16, device="cuda")
     o = torch.empty((B, 128, 128), dtype=torch.bfloat16, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    mla.mla_absorb_q(dev_bf16(x["q_nope"]), dev_bf16(x["q_pe"]), dev_bf16(x["w_uk"]), q)
+    mla.mla_absorb_q(dev_bf16(x["q_nope"]), dev_bf16(x["q_pe"]), dev_bf16(x["w_uk"]), q,
+                     dev_status=status)
     mla.mla_decode(q, dl["cache"], dl["block_table"], dl["seq_lens"], dl["softmax_scale"], out,
                    workspace=mla.make_workspace(B), dev_status=status)
-    mla.mla_absorb_out(out, dev_bf16(x["w_uv"]), o)
+    mla.mla_absorb_out(out, dev_bf16(x["w_uv"]), o, dev_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     q_ref = oracle.absorb_q(x["q_nope"], x["q_pe"], x["w_uk"])
