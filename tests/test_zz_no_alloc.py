@@ -73,3 +73,44 @@ def test_noalloc_rejects_batch_beyond_its_scratch():
                                 ctypes.c_float(0.1), None, None, None, None)
     assert rc == 1
     assert b"MLA_NOALLOC_MAX_BATCH" in lib.mla_last_error_detail()
+
+
+def test_maximum_batch_against_oracle():
+    """The largest batch the library documents (MLA_NOALLOC_MAX_BATCH = 8192
+    requests of 1-24 tokens, page 16): mla_decode with a workspace and
+    mla_decode_noalloc, whose 16 MiB scratch then holds only ~31 of the split
+    ranges, both against the oracle on sampled requests and against each
+    other everywhere."""
+    import mla_latent_cache_decode_gb300 as mla
+    import oracle
+    lib = mla.get_lib()
+    B = 8192
+    rng = np.random.default_rng(8192)
+    lens = rng.integers(1, 25, size=B).tolist()
+    w = mi.custom_workload(lens, block_size=16, append=True, pool_factor=1.2)
+    dl = mi.make_device_layer(w, 0, "cuda", q_kind="sharp")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cache0 = mi.to_bits(dl["cache"])   # the oracle's input: the cache before any GPU work
+    mla.mla_cache_append(dl["kv_new"], dl["slot_mapping"], dl["cache"], dev_status=status)
+    x = dict(q=dl["q"], cache=dl["cache"], bt=dl["block_table"], sl=dl["seq_lens"],
+             scale=dl["softmax_scale"], B=B)
+    out = torch.full((B, 128, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, 128), float("nan"), dtype=torch.float32, device="cuda")
+    mla.mla_decode(x["q"], x["cache"], x["bt"], x["sl"], x["scale"], out, lse, dev_status=status)
+    out_na = torch.full_like(out, float("nan"))
+    lse_na = torch.full_like(lse, float("nan"))
+    rc = _noalloc_via_c_abi(lib, x, out_na, lse_na, status)
+    assert rc == 0, lib.mla_last_error_detail()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert_close(host_f64(out_na), host_f64(out), "noalloc vs mla_decode at 8192 requests")
+    assert_lse_close(lse_na.cpu().numpy(), lse.cpu().numpy())
+    arr = np.array(lens)
+    reqs = sorted({0, 1, B // 2, B - 1, int(arr.argmin()), int(arr.argmax())}
+                  | set(rng.choice(B, 26, replace=False).tolist()))
+    oracle.append(mi.to_bits(dl["kv_new"]), dl["slot_mapping"].cpu().numpy(), cache0)
+    ref, ref_lse = oracle.decode(mi.to_bits(dl["q"][reqs]), cache0, dl["block_table_host"][reqs],
+                                 arr[reqs].astype(np.int32), dl["softmax_scale"])
+    for name, o, l in (("mla_decode", out, lse), ("noalloc", out_na, lse_na)):
+        assert_close(host_f64(o)[reqs], ref, f"{name} at 8192 requests")
+        assert_lse_close(l.cpu().numpy()[reqs], ref_lse)
