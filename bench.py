@@ -221,11 +221,14 @@ def run_mine(args, w, rank, world, local_rank):
     L = w.layers
     scale = mi.SOFTMAX_SCALE
 
+    nvtx = torch.cuda.nvtx
+
     def step(timing_events=None):
         mla.mla_decode_plan(W["seq"], W["bt"], w.block_size, ws, dev_status=status, stream=sh,
                             num_blocks=w.num_blocks())
         for l in range(L):
             d = W["layers"][l]
+            nvtx.range_push(f"layer {l}")
             # mla_decode_append_planned (the append of this step's row fused
             # into the decode kernel), as its two launches so that the decode
             # kernel can be timed on its own
@@ -237,8 +240,22 @@ def run_mine(args, w, rank, world, local_rank):
             if timing_events is not None:
                 timing_events[l][1].record(stream)
             mla.mla_combine_planned(ws, w.batch, W["outs"][l], W["lses"][l], stream=sh)
+            nvtx.range_pop()
 
     launches_per_step = 1 + L * 2
+
+    # Between timed steps the L2 is flushed (a write of 2x its size, outside the
+    # timed events) when one step's cache is small enough to stay partly
+    # resident; a step reading many times L2 flushes it by itself.
+    l2_bytes = torch.cuda.get_device_properties(device).L2_cache_size
+    step_cache = algorithmic_bytes_per_layer(w)[0] * L
+    flush_l2 = step_cache < 8 * l2_bytes
+    flush_buf = (torch.empty(2 * l2_bytes, dtype=torch.uint8, device=device)
+                 if flush_l2 else None)
+
+    def flush():
+        if flush_buf is not None:
+            flush_buf.fill_(0x5A)
 
     for _ in range(args.warmup):
         step()
@@ -265,19 +282,31 @@ def run_mine(args, w, rank, world, local_rank):
         clocks.start()
     barrier()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
+    # each step between its own pair of events; with the flush, the flush
+    # runs between a step's end event and the next step's start event
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush()
+        ev[k][0].record(stream)
         if graph is not None:
             graph.replay()
         else:
             step()
-    e1.record(stream)
+        ev[k][1].record(stream)
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop() if rank == 0 else None
-    ms_total = reduce_max(e0.elapsed_time(e1), world, device)
+    per_step = [a.elapsed_time(b) for a, b in ev]
+    ms_total = reduce_max(sum(per_step), world, device)
     ms_step = ms_total / args.steps
+    per_step_sorted = sorted(per_step)
+
+    def pct(p):
+        return per_step_sorted[min(len(per_step_sorted) - 1, int(p * len(per_step_sorted)))]
+    step_stats = {"median": round(statistics.median(per_step), 4), "p10": round(pct(0.10), 4),
+                  "p90": round(pct(0.90), 4), "min": round(per_step_sorted[0], 4),
+                  "max": round(per_step_sorted[-1], 4)}
     assert int(status.item()) == 0, f"device status {int(status.item())}"
 
     # ---- the same step uncaptured (eager launches), reported beside the graph's
@@ -286,12 +315,15 @@ def run_mine(args, w, rank, world, local_rank):
         k_eager = max(1, min(args.steps, 20))
         torch.cuda.synchronize()
         g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        g0.record(stream)
+        eager = []
         for _ in range(k_eager):
+            flush()
+            g0.record(stream)
             step()
-        g1.record(stream)
-        torch.cuda.synchronize()
-        eager_ms = reduce_max(g0.elapsed_time(g1) / k_eager, world, device)
+            g1.record(stream)
+            torch.cuda.synchronize()
+            eager.append(g0.elapsed_time(g1))
+        eager_ms = reduce_max(statistics.mean(eager), world, device)
 
     # ---- per-launch duration of the decode kernel (events around each launch)
     kev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
@@ -299,6 +331,7 @@ def run_mine(args, w, rank, world, local_rank):
     ksteps = max(1, min(args.steps, 20))
     kms = []
     for _ in range(ksteps):
+        flush()
         step(kev)
         torch.cuda.synchronize()
         kms += [a.elapsed_time(b) for a, b in kev]
@@ -418,13 +451,15 @@ def run_mine(args, w, rank, world, local_rank):
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-        "step_latency_us": round(ms_step * 1e3, 1), "higher_is_better": True,
+        "step_latency_us": round(ms_step * 1e3, 1), "step_ms": step_stats,
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "batch": w.batch, "seq_len": w.seq_lens[0]
                    if len(set(w.seq_lens)) == 1 else "mixed", "layers": L, "heads": 128,
                    "block_size": w.block_size, "cache_gb_per_step": round(step_cache_bytes / 1e9, 4),
-                   "l2": f"inputs larger than L2: {step_cache_bytes / 1e9:.2f} GB of cache per step"
-                   if step_cache_bytes > 256e6 else "L2 not flushed (small workload)",
+                   "l2": (f"flushed: {2 * l2_bytes / 1e6:.0f} MB written between timed steps "
+                          f"(outside their events)") if flush_l2 else
+                         f"inputs larger than L2: {step_cache_bytes / 1e9:.2f} GB of cache per step",
                    "cuda_graph": graph is not None,
                    "parallelism": "dp-attention rank per GPU; replicas only"},
         "step_roofline_frac": round(roofline_step_us / (ms_step * 1e3), 4),

@@ -263,20 +263,31 @@ mla_status_t mla_combine(const float *o_partial, const float *lse_partial,
  * 16 MiB until the process exits.  It calls no cudaMalloc, cudaFree or other
  * allocating routine.
  *
- * Limits: batch <= MLA_NOALLOC_MAX_BATCH (8192), else
- * MLA_ERR_INVALID_ARGUMENT with an explanatory detail.  Because the scratch
- * holds fewer split partials than a full workspace, long contexts are spread
- * over fewer SMs than with mla_decode, which can make it slower; results agree
- * with mla_decode within the library's tolerance (the split points differ, so
- * fp32 rounding differs).
+ * Limits: num_heads must be 128 (the tensor-parallel head counts that
+ * mla_decode accepts pad q into its workspace, which this entry point does
+ * not have; other values return MLA_ERR_UNSUPPORTED); batch <=
+ * MLA_NOALLOC_MAX_BATCH (8192), else MLA_ERR_INVALID_ARGUMENT with an
+ * explanatory detail.  Because the scratch holds fewer split partials than a
+ * full workspace, long contexts are spread over fewer SMs than with
+ * mla_decode, which can make it slower; results agree with mla_decode within
+ * the library's tolerance (the split points differ, so fp32 rounding
+ * differs).
  *
  * Set-up: the first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  Every call shares the one array and overwrites
- * what the previous call left there (each call re-plans and re-zeroes what
- * must start at zero), so calls whose kernels overlap on the GPU — on
- * different streams, or from different host threads — race and give
- * undefined results: serialise them.
+ * (cudaGetSymbolAddress) with that device current.  Under CUDA's lazy module
+ * loading that lookup may be the moment the driver loads the library's
+ * device code and places the 16 MiB array on the device, so the first call
+ * can itself fail with MLA_ERR_CUDA (out of memory).  Make one call per
+ * device at set-up time (any valid call, e.g. batch 1), before any stream
+ * capture and before the serving loop.  The address is kept per device and
+ * looked up again only if the device's context was destroyed and recreated
+ * (cudaDeviceReset); such a call again counts as a first call.
+ *
+ * Sharing: every call shares the one array and overwrites what the previous
+ * call left there (each call re-plans and re-zeroes what must start at
+ * zero), so calls whose kernels overlap on the GPU — on different streams, or
+ * from different host threads — race and give undefined results: serialise
+ * them.
  */
 #define MLA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 #define MLA_NOALLOC_MAX_BATCH 8192

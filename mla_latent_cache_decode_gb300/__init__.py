@@ -181,8 +181,10 @@ def mla_decode_plan(seq_lens, block_table, block_size, workspace, num_heads=NUM_
                                      _ptr(dev_status), _stream(stream)))
 
 
-def _decode(fn, q, cache, block_table, seq_lens, softmax_scale, out, lse, workspace,
-            max_seq_len, dev_status, stream):
+def _check_decode_tensors(q, cache, block_table, seq_lens, out, lse):
+    """dtype, layout and shape checks shared by every decode entry point: the C
+    ABI sees raw pointers, so a mismatched out, lse, seq_lens or block_table
+    would otherwise be read or written past its end on the device."""
     import torch
     _need(q, torch.bfloat16, 3, "q")
     _need(cache, torch.bfloat16, 3, "cache")
@@ -196,6 +198,14 @@ def _decode(fn, q, cache, block_table, seq_lens, softmax_scale, out, lse, worksp
         raise ValueError("shape mismatch: q [B,H,576], cache [NB,BS,576], out [B,H,512]")
     if seq_lens.shape[0] != B or block_table.shape[0] != B:
         raise ValueError("seq_lens / block_table batch mismatch")
+    if lse is not None and tuple(lse.shape) != (B, H):
+        raise ValueError(f"lse must be [B, H] = [{B}, {H}], got {tuple(lse.shape)}")
+    return B, H
+
+
+def _decode(fn, q, cache, block_table, seq_lens, softmax_scale, out, lse, workspace,
+            max_seq_len, dev_status, stream):
+    B, H = _check_decode_tensors(q, cache, block_table, seq_lens, out, lse)
     if max_seq_len is None:
         max_seq_len = block_table.shape[1] * cache.shape[1]
     _check(fn(_ptr(q), _ptr(cache), cache.shape[0], cache.shape[1], _ptr(block_table),
@@ -286,17 +296,10 @@ def mla_combine(o_partial, lse_partial, split_offsets, out, lse=None, stream=Non
 def mla_decode_noalloc(q, cache, block_table, seq_lens, softmax_scale, out, lse=None,
                        max_seq_len=None, dev_status=None, stream=None):
     """mla_decode without a workspace, for callers that cannot allocate device
-    memory: the library's fixed 16 MiB scratch array stands in for it (batch
-    <= 8192; calls must not overlap on the GPU)."""
-    import torch
-    _need(q, torch.bfloat16, 3, "q")
-    _need(cache, torch.bfloat16, 3, "cache")
-    _need(block_table, torch.int32, 2, "block_table")
-    _need(seq_lens, torch.int32, 1, "seq_lens")
-    _need(out, torch.bfloat16, 3, "out")
-    if lse is not None:
-        _need(lse, torch.float32, 2, "lse")
-    B, H, _ = q.shape
+    memory: the library's fixed 16 MiB scratch array stands in for it (128
+    heads, batch <= 8192; make a first call per device at set-up; calls must
+    not overlap on the GPU)."""
+    B, H = _check_decode_tensors(q, cache, block_table, seq_lens, out, lse)
     if max_seq_len is None:
         max_seq_len = block_table.shape[1] * cache.shape[1]
     _check(get_lib().mla_decode_noalloc(

@@ -24,6 +24,7 @@
 
 #include "common.cuh"
 #include "sm100.cuh"
+#include "trace.h"
 
 namespace mla {
 void set_error_detail(const char *msg);
@@ -387,6 +388,7 @@ extern "C" {
 
 mla_status_t mla_absorb_q(const void *q_nope, const void *q_pe, const void *w_uk, int32_t batch,
                           int32_t num_heads, void *q, int32_t *dev_status, void *stream) {
+  TraceRange trace_range("mla_absorb_q");
   set_error_detail("");
   const void *ptrs[4] = {q_nope, q_pe, w_uk, q};
   mla_status_t s = check(ptrs, 4, batch, num_heads);
@@ -399,6 +401,7 @@ mla_status_t mla_absorb_q(const void *q_nope, const void *q_pe, const void *w_uk
 
 mla_status_t mla_absorb_out(const void *out, const void *w_uv, int32_t batch, int32_t num_heads,
                             void *o, int32_t *dev_status, void *stream) {
+  TraceRange trace_range("mla_absorb_out");
   set_error_detail("");
   const void *ptrs[3] = {out, w_uv, o};
   mla_status_t s = check(ptrs, 3, batch, num_heads);

@@ -7,6 +7,7 @@
 #include <string>
 
 #include "common.cuh"
+#include "trace.h"
 
 namespace mla {
 cudaError_t launch_cache_append(const void *kv_new, const int64_t *slots, int64_t num_tokens,
@@ -155,6 +156,7 @@ int mla_abi_version(void) { return MLA_ABI_VERSION; }
 mla_status_t mla_cache_append(const void *kv_new, const int64_t *slot_mapping, int64_t num_tokens,
                               void *cache, int64_t num_blocks, int32_t block_size,
                               int32_t *dev_status, void *stream) {
+  TraceRange trace_range("mla_cache_append");
   g_detail.clear();
   if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARGUMENT, "num_tokens < 0");
   if (block_size <= 0) return fail(MLA_ERR_INVALID_ARGUMENT, "block_size %d <= 0", block_size);
@@ -181,6 +183,7 @@ mla_status_t mla_decode_plan(const int32_t *seq_lens, const int32_t *block_table
                              int32_t num_heads, int32_t max_blocks_per_seq, int32_t block_size,
                              int64_t num_blocks, void *workspace, size_t workspace_bytes,
                              int32_t *dev_status, void *stream) {
+  TraceRange trace_range("mla_decode_plan");
   g_detail.clear();
   if (batch < 0) return fail(MLA_ERR_INVALID_ARGUMENT, "batch < 0");
   if (num_heads < 1 || num_heads > kHeads)
@@ -211,6 +214,7 @@ mla_status_t mla_decode_partial(const void *q, void *cache, const void *kv_new,
                                 int32_t max_seq_len, float softmax_scale, void *out, float *lse,
                                 void *workspace, size_t workspace_bytes, int32_t *dev_status,
                                 void *stream) {
+  TraceRange trace_range("mla_decode_partial");
   g_detail.clear();
   if (need_all_heads(num_heads) != MLA_OK) return MLA_ERR_UNSUPPORTED;
   mla_status_t s = check_decode_args(q, cache, num_blocks, block_size, block_table,
@@ -232,6 +236,7 @@ mla_status_t mla_decode_append_planned(const void *q, void *cache, const void *k
                                        int32_t max_seq_len, float softmax_scale, void *out,
                                        float *lse, void *workspace, size_t workspace_bytes,
                                        int32_t *dev_status, void *stream) {
+  TraceRange trace_range("mla_decode_append_planned");
   if (!kv_new) {
     g_detail.clear();
     return fail(MLA_ERR_INVALID_ARGUMENT, "kv_new is null");
@@ -246,6 +251,7 @@ mla_status_t mla_decode_append_planned(const void *q, void *cache, const void *k
 
 mla_status_t mla_combine_planned(void *workspace, size_t workspace_bytes, int32_t batch,
                                  int32_t num_heads, void *out, float *lse, void *stream) {
+  TraceRange trace_range("mla_combine_planned");
   g_detail.clear();
   if (batch < 0) return fail(MLA_ERR_INVALID_ARGUMENT, "batch < 0");
   if (num_heads != kHeads) return fail(MLA_ERR_UNSUPPORTED, "num_heads must be %d", kHeads);
@@ -268,6 +274,7 @@ mla_status_t mla_decode_planned(const void *q, const void *cache, int64_t num_bl
                                 int32_t batch, int32_t num_heads, int32_t max_seq_len,
                                 float softmax_scale, void *out, float *lse, void *workspace,
                                 size_t workspace_bytes, int32_t *dev_status, void *stream) {
+  TraceRange trace_range("mla_decode_planned");
   if (num_heads != kHeads) {  // a tensor-parallel rank's heads, padded to 128
     g_detail.clear();
     mla_status_t st = check_decode_args(q, cache, num_blocks, block_size, block_table,
@@ -312,6 +319,7 @@ mla_status_t mla_decode(const void *q, const void *cache, int64_t num_blocks, in
                         int32_t max_seq_len, float softmax_scale, void *out, float *lse,
                         void *workspace, size_t workspace_bytes, int32_t *dev_status,
                         void *stream) {
+  TraceRange trace_range("mla_decode");
   g_detail.clear();
   mla_status_t s = check_decode_args(q, cache, num_blocks, block_size, block_table,
                                      max_blocks_per_seq, seq_lens, batch, num_heads, max_seq_len,
@@ -328,6 +336,7 @@ mla_status_t mla_decode(const void *q, const void *cache, int64_t num_blocks, in
 mla_status_t mla_combine(const float *o_partial, const float *lse_partial,
                          const int32_t *split_offsets, int32_t batch, int32_t num_heads,
                          void *out, float *lse, void *stream) {
+  TraceRange trace_range("mla_combine");
   g_detail.clear();
   if (batch < 0 || num_heads <= 0)
     return fail(MLA_ERR_INVALID_ARGUMENT, "batch %d, num_heads %d", batch, num_heads);
@@ -344,6 +353,7 @@ mla_status_t mla_combine(const float *o_partial, const float *lse_partial,
 
 mla_status_t mla_selftest_wait_timeout(uint64_t budget_ns, int32_t *dev_status,
                                        uint64_t *elapsed_ns, void *stream) {
+  TraceRange trace_range("mla_selftest_wait_timeout");
   g_detail.clear();
   if (budget_ns < 1000 || budget_ns > 1000000000ull)
     return fail(MLA_ERR_INVALID_ARGUMENT, "budget_ns %llu: 1 us to 1 s",

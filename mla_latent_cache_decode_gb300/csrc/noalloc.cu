@@ -1,6 +1,8 @@
 // mla_decode_noalloc: the decode entry point for callers that cannot allocate
 // device memory.  Its scratch (split plan + partial results) lives in a fixed,
 // file-scope device array instead of a caller-provided workspace.
+#include <cuda.h>
+
 #include <cmath>
 #include <mutex>
 
@@ -28,27 +30,64 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[MLA_NOALLOC_SCR
 
 namespace {
 
-// Device address of g_noalloc_scratch, looked up once per device with that
-// device current.  In host code the symbol itself is only a host-side
-// stand-in, never a device address.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+// Unique id of the current CUDA context (0 if it cannot be read).  A context
+// that is destroyed and created again (cudaDeviceReset, then any runtime call)
+// gets a new id, and the module holding g_noalloc_scratch is loaded anew in it.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = (CtxGetCurrentFn)p;
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = (CtxGetIdFn)p;
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of g_noalloc_scratch, looked up with cudaGetSymbolAddress
+// once per device (with that device current) and kept with the id of the
+// context it was looked up in.  In host code the symbol itself is only a
+// host-side stand-in, never a device address.  If the device's context has
+// changed since (a reset), the address is looked up again: the old one
+// belonged to the destroyed context.
 void *scratch_address(int *err) {
   static std::mutex mu;
   static void *addr[64] = {nullptr};
+  static unsigned long long ctx_of[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0 || dev >= 64) {
     *err = 1;
     return nullptr;
   }
+  // the first runtime call above made the device's primary context current
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
+  if (!addr[dev] || ctx == 0 || ctx != ctx_of[dev]) {
     void *p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || !p) {
       *err = 2;
+      addr[dev] = nullptr;
       return nullptr;
     }
     addr[dev] = p;
+    ctx_of[dev] = ctx;
   }
   *err = 0;
   return addr[dev];

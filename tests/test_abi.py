@@ -123,3 +123,18 @@ def test_partial_entry_points_need_all_heads(lib):
     lib.mla_decode_workspace_size.argtypes = [i32, i32]
     lib.mla_decode_workspace_size.restype = sz
     assert lib.mla_decode_workspace_size(4, 129) == 0
+
+
+def test_noalloc_host_validation(lib):
+    P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    lib.mla_decode_noalloc.argtypes = [P, P, i64, i32, P, i32, P, i32, i32, i32, f32, P, P, P, P]
+    lib.mla_decode_noalloc.restype = ctypes.c_int
+    lib.mla_last_error_detail.restype = ctypes.c_char_p
+    call = lambda batch, heads: lib.mla_decode_noalloc(None, None, 1, 64, None, 1, None, batch,
+                                                       heads, 64, 0.1, None, None, None, None)
+    assert call(8193, 128) == 1                      # beyond the fixed scratch's batch limit
+    assert b"MLA_NOALLOC_MAX_BATCH" in lib.mla_last_error_detail()
+    assert call(4, 16) == 2                          # only the kernel's 128 heads
+    assert b"num_heads" in lib.mla_last_error_detail()
+    assert call(-1, 128) == 1
+    assert call(0, 128) == 0                         # empty batch: valid no-op, nothing touched

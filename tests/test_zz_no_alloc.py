@@ -30,14 +30,15 @@ def _inputs(lens, block_size, seed, q_kind):
                 scale=d["softmax_scale"], B=len(lens))
 
 
-def _noalloc_via_c_abi(lib, x, out, lse, status):
+def _noalloc_via_c_abi(lib, x, out, lse, status, heads=128):
     stream = torch.cuda.current_stream().cuda_stream
     return lib.mla_decode_noalloc(
         ctypes.c_void_p(x["q"].data_ptr()), ctypes.c_void_p(x["cache"].data_ptr()),
         x["cache"].shape[0], x["cache"].shape[1], ctypes.c_void_p(x["bt"].data_ptr()),
-        x["bt"].shape[1], ctypes.c_void_p(x["sl"].data_ptr()), x["B"], 128,
+        x["bt"].shape[1], ctypes.c_void_p(x["sl"].data_ptr()), x["B"], heads,
         x["bt"].shape[1] * x["cache"].shape[1], ctypes.c_float(x["scale"]),
-        ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(lse.data_ptr()),
+        ctypes.c_void_p(out.data_ptr()),
+        ctypes.c_void_p(lse.data_ptr()) if lse is not None else None,
         ctypes.c_void_p(status.data_ptr()), ctypes.c_void_p(stream))
 
 
@@ -73,6 +74,49 @@ def test_noalloc_rejects_batch_beyond_its_scratch():
                                 ctypes.c_float(0.1), None, None, None, None)
     assert rc == 1
     assert b"MLA_NOALLOC_MAX_BATCH" in lib.mla_last_error_detail()
+
+
+def test_noalloc_rejects_other_head_counts_on_the_host():
+    """Only the kernel's 128 heads: a tensor-parallel rank's 16 heads would need
+    q padded into a workspace, which this entry point does not have."""
+    import mla_latent_cache_decode_gb300 as mla
+    lib = mla.get_lib()
+    x = _inputs([5, 70], 16, 33, "normal")
+    out = torch.empty((x["B"], 128, 512), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert _noalloc_via_c_abi(lib, x, out, None, status, heads=16) == 2
+    assert b"num_heads" in lib.mla_last_error_detail()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+
+
+def test_noalloc_without_lse_and_at_an_intermediate_batch():
+    """lse = NULL, and a 4096-request batch holding one long-context request:
+    the fixed scratch then holds fewer split ranges than mla_decode's workspace
+    (one per SM pair), so the plans differ; the results agree within the
+    tolerance, and out written with lse = NULL equals out written with it."""
+    import mla_latent_cache_decode_gb300 as mla
+    lib = mla.get_lib()
+    rng = np.random.default_rng(4096)
+    lens = rng.integers(1, 100, size=4096).tolist()
+    lens[1234] = 30000
+    x = _inputs(lens, 32, 34, "sharp")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out_nolse = torch.full((x["B"], 128, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    assert _noalloc_via_c_abi(lib, x, out_nolse, None, status) == 0, lib.mla_last_error_detail()
+    out = torch.full_like(out_nolse, float("nan"))
+    lse = torch.full((x["B"], 128), float("nan"), dtype=torch.float32, device="cuda")
+    assert _noalloc_via_c_abi(lib, x, out, lse, status) == 0, lib.mla_last_error_detail()
+    ref = torch.empty_like(out)
+    ref_lse = torch.empty_like(lse)
+    mla.mla_decode(x["q"], x["cache"], x["bt"], x["sl"], x["scale"], ref, ref_lse,
+                   dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(out_nolse.view(torch.int16), out.view(torch.int16))
+    assert_close(host_f64(out), host_f64(ref), "noalloc vs mla_decode, 4096 requests")
+    assert_close(host_f64(out[1234]), host_f64(ref[1234]), "the 30000-token request")
+    assert_lse_close(lse.cpu().numpy(), ref_lse.cpu().numpy())
 
 
 def test_maximum_batch_against_oracle():
