@@ -299,45 +299,51 @@ __device__ __forceinline__ void combine_row(const float *__restrict__ o_part,
 }
 
 // Merges the partials of every split request of a plan.  The decode stores
-// them as [slot][512 / 4][128][4], so in the block of (request, 16-dim block)
-// thread h = head reads four dims of its head per load (a warp's loads are
-// 512 contiguous bytes) and accumulates its 16 dims in registers; splits are
-// taken four at a time with all their loads (log-sum-exps and data) issued
-// before any is used, since the kernel is latency-bound, and the split's
-// slots come from the plan's per-request record without any division.  The bf16 results are transposed through
-// shared memory into the [B][H][512] output (32 bytes of a row per head).
-// grid = (batch, 512 / 16), 128 threads.
+// them as [slot][512 / 4][128][4].  A block takes one request and 16 output
+// dims.  With one split lane (kLanes = 1) its thread h is head h and merges
+// all the request's splits, four at a time with their loads all in flight
+// before any is used (a warp's float4 loads are 512 contiguous bytes of 32
+// heads).  With four split lanes (kLanes = 4; for small batches, whose
+// requests are spread over many ranges) a block takes 32 heads, and warp s
+// merges splits s, s + 4, s + 8, ... of them; the four running results of a
+// head (max, weight sum, 16 weighted dims) are then merged through shared
+// memory, one warp per four dims.  The bf16 results leave as 32-byte row
+// pieces.  grid = (batch, 512 / 16, kLanes), 128 threads.
 constexpr int kCombDims = 16;
-constexpr int kCombGroup = 4;  // splits whose loads are in flight together
+constexpr int kCombGroup = 4;  // splits per lane whose loads are in flight together
 
+template <int kLanes>
 __global__ void __launch_bounds__(kHeads) plan_combine_kernel(void *ws, int32_t batch,
                                                               int32_t max_ranges,
                                                               __nv_bfloat16 *__restrict__ out,
                                                               float *__restrict__ lse) {
+  constexpr int kBlockHeads = kHeads / kLanes;
   PlanView v = plan_view(ws, batch, kHeads, max_ranges);
-  const int b = blockIdx.x, d0 = blockIdx.y * kCombDims, h = threadIdx.x;
+  const int b = blockIdx.x, d0 = blockIdx.y * kCombDims;
+  const int sl = kLanes == 1 ? 0 : (int)(threadIdx.x >> 5);  // split lane
+  const int hb = kLanes == 1 ? (int)threadIdx.x : (int)(threadIdx.x & 31);  // head in the block
+  const int h = blockIdx.z * kBlockHeads + hb;
   const ReqSplit rs = v.req_split[b];
   if (rs.p0 == rs.p1) return;  // not split (or empty): the decode wrote it
   const int nsplit = rs.p1 - rs.p0 + 1;
   auto slot_of_split = [&](int k) -> int64_t {
     return k == 0 ? 2 * rs.p0 + rs.first_odd : 2 * (rs.p0 + k);
   };
-  __shared__ __align__(16) __nv_bfloat16 tile[kHeads][kCombDims + 8];  // +8: stagger the rows
+  __shared__ __align__(16) __nv_bfloat16 tile[kBlockHeads][kCombDims + 8];  // +8: stagger
   float4 acc[kCombDims / 4];
 #pragma unroll
   for (int j = 0; j < kCombDims / 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
   float m = -INFINITY, z = 0.f;
-  // splits kCombGroup at a time, all their loads issued before any is used (the
-  // kernel is latency-bound); the running max rescales what was summed so far
-  for (int k0 = 0; k0 < nsplit; k0 += kCombGroup) {
+  // this lane's splits kCombGroup at a time; the running max rescales what
+  // was summed so far
+  for (int k0 = sl; k0 < nsplit; k0 += kLanes * kCombGroup) {
     float l[kCombGroup];
-#pragma unroll
-    for (int u = 0; u < kCombGroup; ++u)
-      l[u] = k0 + u < nsplit ? v.lse_part[slot_of_split(k0 + u) * kHeads + h] : -INFINITY;
     float4 x[kCombGroup][kCombDims / 4];
 #pragma unroll
     for (int u = 0; u < kCombGroup; ++u) {
-      const int64_t w = slot_of_split(k0 + u < nsplit ? k0 + u : k0);
+      const int k = k0 + u * kLanes;
+      const int64_t w = slot_of_split(k < nsplit ? k : k0);  // k0 < nsplit: a valid slot
+      l[u] = k < nsplit ? v.lse_part[w * kHeads + h] : -INFINITY;
       const float4 *src = reinterpret_cast<const float4 *>(v.o_part) +
                           (w * (kVDim / 4) + d0 / 4) * kHeads + h;
 #pragma unroll
@@ -367,34 +373,75 @@ __global__ void __launch_bounds__(kHeads) plan_combine_kernel(void *ws, int32_t 
       }
     }
   }
-  const float inv = z > 0.f ? 1.f / z : 0.f;
+  if constexpr (kLanes == 1) {
+    const float inv = z > 0.f ? 1.f / z : 0.f;
 #pragma unroll
-  for (int j = 0; j < kCombDims / 4; ++j) {
-    *reinterpret_cast<__nv_bfloat162 *>(&tile[h][4 * j]) =
-        __floats2bfloat162_rn(acc[j].x * inv, acc[j].y * inv);
-    *reinterpret_cast<__nv_bfloat162 *>(&tile[h][4 * j + 2]) =
-        __floats2bfloat162_rn(acc[j].z * inv, acc[j].w * inv);
+    for (int j = 0; j < kCombDims / 4; ++j) {
+      *reinterpret_cast<__nv_bfloat162 *>(&tile[hb][4 * j]) =
+          __floats2bfloat162_rn(acc[j].x * inv, acc[j].y * inv);
+      *reinterpret_cast<__nv_bfloat162 *>(&tile[hb][4 * j + 2]) =
+          __floats2bfloat162_rn(acc[j].z * inv, acc[j].w * inv);
+    }
+    if (lse && blockIdx.y == 0) lse[(int64_t)b * kHeads + h] = z > 0.f ? m + logf(z) : -INFINITY;
+  } else {
+    __shared__ float s_m[kLanes][kBlockHeads], s_z[kLanes][kBlockHeads];
+    __shared__ float4 s_acc[kLanes][kCombDims / 4][kBlockHeads];
+    s_m[sl][hb] = m;
+    s_z[sl][hb] = z;
+#pragma unroll
+    for (int j = 0; j < kCombDims / 4; ++j) s_acc[sl][j][hb] = acc[j];
+    __syncthreads();
+    // warp sl finishes dims [4 sl, 4 sl + 4) of the block's heads
+    float M = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kLanes; ++i) M = fmaxf(M, s_m[i][hb]);
+    float Z = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int i = 0; i < kLanes; ++i) {
+        const float mi = s_m[i][hb];
+        const float a = mi == -INFINITY ? 0.f : __expf(mi - M);
+        const float4 xx = s_acc[i][sl][hb];
+        Z += a * s_z[i][hb];
+        o.x += a * xx.x; o.y += a * xx.y; o.z += a * xx.z; o.w += a * xx.w;
+      }
+    }
+    const float inv = Z > 0.f ? 1.f / Z : 0.f;
+    *reinterpret_cast<__nv_bfloat162 *>(&tile[hb][4 * sl]) =
+        __floats2bfloat162_rn(o.x * inv, o.y * inv);
+    *reinterpret_cast<__nv_bfloat162 *>(&tile[hb][4 * sl + 2]) =
+        __floats2bfloat162_rn(o.z * inv, o.w * inv);
+    if (lse && blockIdx.y == 0 && sl == 0)
+      lse[(int64_t)b * kHeads + h] = Z > 0.f ? M + logf(Z) : -INFINITY;
   }
   __syncthreads();
-  // 128 rows x (2 kCombDims) bytes: kCombDims / 8 pieces of 16 bytes per row,
-  // thread t takes pieces t + 128 k
+  // kBlockHeads rows x (2 kCombDims) bytes, in 16-byte pieces
   constexpr int kPieces = kCombDims / 8;
-  __nv_bfloat16 *orow = out + (int64_t)b * kHeads * kVDim + d0;
-#pragma unroll
-  for (int k = 0; k < kPieces; ++k) {
-    const int piece = h + kHeads * k, row = piece / kPieces, part = piece % kPieces;
-    *reinterpret_cast<uint4 *>(orow + (int64_t)row * kVDim + part * 8) =
+  for (int piece = threadIdx.x; piece < kBlockHeads * kPieces; piece += kHeads) {
+    const int row = piece / kPieces, part = piece % kPieces;
+    __nv_bfloat16 *orow =
+        out + ((int64_t)b * kHeads + blockIdx.z * kBlockHeads + row) * kVDim + d0;
+    *reinterpret_cast<uint4 *>(orow + part * 8) =
         *reinterpret_cast<const uint4 *>(&tile[row][part * 8]);
   }
-  if (lse && blockIdx.y == 0) lse[(int64_t)b * kHeads + h] = z > 0.f ? m + logf(z) : -INFINITY;
 }
 
 cudaError_t launch_plan_combine(void *ws, int32_t batch, int32_t heads, int32_t max_ranges,
                                 void *out, float *lse, cudaStream_t stream) {
   if (heads != kHeads) return cudaErrorInvalidValue;
-  dim3 grid(batch, kVDim / kCombDims);
-  plan_combine_kernel<<<grid, kHeads, 0, stream>>>(ws, batch, max_ranges,
-                                                   (__nv_bfloat16 *)out, lse);
+  // Four split lanes when requests average eight or more ranges (a small
+  // batch, where one long request is spread over most of the SM pairs); one
+  // otherwise, so that an ordinary batch keeps one block per 16 dims.
+  if ((int64_t)batch * 8 <= max_ranges) {
+    dim3 grid(batch, kVDim / kCombDims, 4);
+    plan_combine_kernel<4><<<grid, kHeads, 0, stream>>>(ws, batch, max_ranges,
+                                                        (__nv_bfloat16 *)out, lse);
+  } else {
+    dim3 grid(batch, kVDim / kCombDims, 1);
+    plan_combine_kernel<1><<<grid, kHeads, 0, stream>>>(ws, batch, max_ranges,
+                                                        (__nv_bfloat16 *)out, lse);
+  }
   return cudaGetLastError();
 }
 
