@@ -247,6 +247,67 @@ mla_status_t mla_combine(const float *o_partial, const float *lse_partial,
                          void *out, float *lse, void *stream);
 
 /*
+ * FP8 latent cache — mla_cache_append_fp8, mla_decode_fp8, mla_decode_fp8_planned.
+ *
+ * Defined by: an FP8 MLA cache holds one byte per latent element, 576 bytes
+ * per token per layer, half the bf16 cache [MLA 的 TP 切分 (10100.com),
+ * opening paragraph (32 KB -> 576 bytes per token per layer) and section 5.1
+ * ("576 bytes in FP8")].  The pages name no format, scale or rounding; this
+ * library reads them as:
+ *   - format: OCP FP8 E4M3 (bias 7, 3 mantissa bits, no infinities, code
+ *     S.1111.111 is NaN, largest finite magnitude 448);
+ *   - one scale per layer, kv_scale > 0 and finite (1 when unused): a stored
+ *     code c stands for value(c) * kv_scale, so a row stays 576 bytes;
+ *   - a new bf16 element x is stored as the code nearest to
+ *     fp32(x) * fp32(1 / kv_scale) (one fp32 rounding each), ties to the even
+ *     code, magnitudes above 448 saturating to 448, NaN to NaN.
+ * Decode computes the same softmax attention as mla_decode (the equation at
+ * the top of this file) over rows whose elements are value(code) * kv_scale.
+ * The tensor cores run it on f16 operands, which hold every E4M3 value
+ * exactly; q is taken to f16 inside the kernel, exactly for |q| in
+ * [2^-14, 65504] (smaller magnitudes round to f16 subnormals, larger ones
+ * saturate), so q must lie within 65504 in magnitude.
+ *
+ * mla_cache_append_fp8 — as mla_cache_append, storing each bf16 row of kv_new
+ * (bf16 [num_tokens, 576]) quantised into cache8 (uint8 [num_blocks,
+ * block_size, 576]) at its slot (-1 = skip; out-of-pool slots are skipped and
+ * reported as MLA_ERR_DEVICE_RANGE in *dev_status).
+ *
+ * mla_decode_fp8 — mla_decode over cache8: plans (as mla_decode_plan, with the
+ * table), decodes and merges split partials.  num_heads must be 128.
+ *
+ * mla_decode_fp8_planned — the same with the plan already in the workspace
+ * (mla_decode_plan with the same lengths, table and sizes).  With kv_new
+ * non-null (bf16 [batch, 576]) it first stores kv_new[b], quantised as above,
+ * at position seq_lens[b] - 1 of request b inside the decode kernel, as
+ * mla_decode_append_planned does for a bf16 cache.
+ *
+ * Arguments not listed are those of mla_decode / mla_decode_planned, with the
+ * same layout, ownership and requirements (cache8 16-byte aligned; block_size
+ * in {16, 32, 64, 128, 256}).  Returns MLA_OK, MLA_ERR_INVALID_ARGUMENT
+ * (including a kv_scale that is not positive and finite),
+ * MLA_ERR_UNSUPPORTED (num_heads != 128), MLA_ERR_WORKSPACE_TOO_SMALL or
+ * MLA_ERR_CUDA; device faults go to *dev_status as for mla_decode.
+ */
+mla_status_t mla_cache_append_fp8(const void *kv_new, const int64_t *slot_mapping,
+                                  int64_t num_tokens, void *cache8, int64_t num_blocks,
+                                  int32_t block_size, float kv_scale, int32_t *dev_status,
+                                  void *stream);
+mla_status_t mla_decode_fp8(const void *q, const void *cache8, int64_t num_blocks,
+                            int32_t block_size, const int32_t *block_table,
+                            int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t batch,
+                            int32_t num_heads, int32_t max_seq_len, float softmax_scale,
+                            float kv_scale, void *out, float *lse, void *workspace,
+                            size_t workspace_bytes, int32_t *dev_status, void *stream);
+mla_status_t mla_decode_fp8_planned(const void *q, void *cache8, const void *kv_new,
+                                    int64_t num_blocks, int32_t block_size,
+                                    const int32_t *block_table, int32_t max_blocks_per_seq,
+                                    const int32_t *seq_lens, int32_t batch, int32_t num_heads,
+                                    int32_t max_seq_len, float softmax_scale, float kv_scale,
+                                    void *out, float *lse, void *workspace, size_t workspace_bytes,
+                                    int32_t *dev_status, void *stream);
+
+/*
  * mla_decode_noalloc — mla_decode for callers that cannot allocate device
  * memory.  The pages have no counterpart to this entry point; it exists for
  * users of this library.

@@ -225,6 +225,33 @@ def make_device_layer(w: Workload, layer: int, device, q_kind="normal", num_head
                 kv_new=kv_new, slot_mapping=slots_t, softmax_scale=SOFTMAX_SCALE)
 
 
+# ----------------------------------------------------------------------------- FP8 cache
+
+def e4m3_codes(x) -> np.ndarray:
+    """E4M3 byte codes of fp32 samples, drawn by torch's float8_e4m3fn cast
+    (an input-drawing step like the bf16 rounding above; NaN stays NaN)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def make_host_layer_fp8(w: Workload, rng, q_kind="normal", num_heads=NUM_HEADS):
+    """make_host_layer with the cache as E4M3 codes (uint8 [NB, BS, 576]) of
+    the same N(0,1) rows; unowned rows and the slot the append will write
+    hold the NaN code."""
+    d = make_host_layer(w, rng, q_kind, num_heads)
+    d["cache8"] = e4m3_codes(bf16_bits_to_f32(d["cache"]))
+    return d
+
+
+def make_device_layer_fp8(w: Workload, layer: int, device, q_kind="normal", block_table=None):
+    """make_device_layer with the cache as E4M3 codes (torch uint8), drawn on the device."""
+    import torch
+    d = make_device_layer(w, layer, device, q_kind=q_kind, block_table=block_table)
+    d["cache8"] = d.pop("cache").float().to(torch.float8_e4m3fn).view(torch.uint8)
+    return d
+
+
 def to_bits(t) -> np.ndarray:
     """Host uint16 bit patterns of a bfloat16 torch tensor."""
     import torch

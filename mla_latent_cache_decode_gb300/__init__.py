@@ -30,7 +30,8 @@ EXPORTED = ("mla_status_string", "mla_last_error_detail", "mla_abi_version", "ml
             "mla_decode_workspace_size", "mla_decode_plan", "mla_decode", "mla_decode_planned",
             "mla_combine", "mla_decode_noalloc", "mla_decode_partial", "mla_combine_planned",
             "mla_decode_append_planned", "mla_place_requests", "mla_place_one", "mla_absorb_q",
-            "mla_absorb_out", "mla_selftest_wait_timeout")
+            "mla_absorb_out", "mla_selftest_wait_timeout", "mla_cache_append_fp8",
+            "mla_decode_fp8", "mla_decode_fp8_planned")
 
 
 class MlaError(RuntimeError):
@@ -84,6 +85,14 @@ def _load():
     lib.mla_absorb_q.restype = ctypes.c_int
     lib.mla_absorb_out.argtypes = [P, P, i32, i32, P, P, P]
     lib.mla_absorb_out.restype = ctypes.c_int
+    lib.mla_cache_append_fp8.argtypes = [P, P, i64, P, i64, i32, f32, P, P]
+    lib.mla_cache_append_fp8.restype = ctypes.c_int
+    lib.mla_decode_fp8.argtypes = [P, P, i64, i32, P, i32, P, i32, i32, i32, f32, f32, P, P, P, sz,
+                                   P, P]
+    lib.mla_decode_fp8.restype = ctypes.c_int
+    lib.mla_decode_fp8_planned.argtypes = [P, P, P, i64, i32, P, i32, P, i32, i32, i32, f32, f32,
+                                           P, P, P, sz, P, P]
+    lib.mla_decode_fp8_planned.restype = ctypes.c_int
     lib.mla_selftest_wait_timeout.argtypes = [ctypes.c_uint64, P, P, P]
     lib.mla_selftest_wait_timeout.restype = ctypes.c_int
     return lib
@@ -306,6 +315,78 @@ def mla_decode_noalloc(q, cache, block_table, seq_lens, softmax_scale, out, lse=
         _ptr(q), _ptr(cache), cache.shape[0], cache.shape[1], _ptr(block_table),
         block_table.shape[1], _ptr(seq_lens), B, H, int(max_seq_len), float(softmax_scale),
         _ptr(out), _ptr(lse), _ptr(dev_status), _stream(stream)))
+    return out
+
+
+def mla_cache_append_fp8(kv_new, slot_mapping, cache8, kv_scale=1.0, dev_status=None,
+                         stream=None):
+    """Quantise each bf16 row of kv_new into the FP8 (E4M3) cache at its slot
+    (code nearest to x / kv_scale, ties to even, saturating to 448)."""
+    import torch
+    _need(kv_new, torch.bfloat16, 2, "kv_new")
+    _need(slot_mapping, torch.int64, 1, "slot_mapping")
+    _need(cache8, torch.uint8, 3, "cache8")
+    if kv_new.shape[1] != ROW_DIM or cache8.shape[2] != ROW_DIM:
+        raise ValueError("rows must be 576 wide")
+    if slot_mapping.shape[0] != kv_new.shape[0]:
+        raise ValueError("slot_mapping and kv_new disagree on the token count")
+    _check(get_lib().mla_cache_append_fp8(_ptr(kv_new), _ptr(slot_mapping), kv_new.shape[0],
+                                          _ptr(cache8), cache8.shape[0], cache8.shape[1],
+                                          float(kv_scale), _ptr(dev_status), _stream(stream)))
+
+
+def mla_decode_fp8(q, cache8, block_table, seq_lens, softmax_scale, out, lse=None,
+                   kv_scale=1.0, workspace=None, max_seq_len=None, dev_status=None, stream=None):
+    """Absorbed-form MLA decode over an FP8 (E4M3) cache: row elements are
+    value(code) * kv_scale (plans, decodes, merges)."""
+    return _decode_fp8(get_lib().mla_decode_fp8, None, q, cache8, block_table, seq_lens,
+                       softmax_scale, out, lse, kv_scale, workspace, max_seq_len, dev_status,
+                       stream)
+
+
+def mla_decode_fp8_planned(q, cache8, block_table, seq_lens, softmax_scale, out, lse=None,
+                           kv_scale=1.0, workspace=None, max_seq_len=None, dev_status=None,
+                           stream=None, kv_new=None):
+    """mla_decode_fp8 with the plan already in `workspace`; with kv_new (bf16 [B, 576]) each
+    request's new row is quantised into the cache first, inside the decode kernel."""
+    return _decode_fp8(get_lib().mla_decode_fp8_planned, kv_new, q, cache8, block_table,
+                       seq_lens, softmax_scale, out, lse, kv_scale, workspace, max_seq_len,
+                       dev_status, stream)
+
+
+def _decode_fp8(fn, kv_new, q, cache8, block_table, seq_lens, softmax_scale, out, lse, kv_scale,
+                workspace, max_seq_len, dev_status, stream):
+    import torch
+    _need(q, torch.bfloat16, 3, "q")
+    _need(cache8, torch.uint8, 3, "cache8")
+    _need(block_table, torch.int32, 2, "block_table")
+    _need(seq_lens, torch.int32, 1, "seq_lens")
+    _need(out, torch.bfloat16, 3, "out")
+    if lse is not None:
+        _need(lse, torch.float32, 2, "lse")
+    B, H, row = q.shape
+    if row != ROW_DIM or cache8.shape[2] != ROW_DIM or tuple(out.shape) != (B, H, KV_LORA_RANK):
+        raise ValueError("shape mismatch: q [B,H,576], cache8 [NB,BS,576], out [B,H,512]")
+    if seq_lens.shape[0] != B or block_table.shape[0] != B:
+        raise ValueError("seq_lens / block_table batch mismatch")
+    if lse is not None and tuple(lse.shape) != (B, H):
+        raise ValueError(f"lse must be [B, H] = [{B}, {H}], got {tuple(lse.shape)}")
+    if kv_new is not None:
+        _need(kv_new, torch.bfloat16, 2, "kv_new")
+        if tuple(kv_new.shape) != (B, ROW_DIM):
+            raise ValueError("kv_new must be [B, 576]")
+    if workspace is None:
+        workspace = make_workspace(B, H, q.device)
+    if max_seq_len is None:
+        max_seq_len = block_table.shape[1] * cache8.shape[1]
+    args = [_ptr(q), _ptr(cache8)]
+    if kv_new is not None or fn is get_lib().mla_decode_fp8_planned:
+        args.append(_ptr(kv_new))
+    args += [cache8.shape[0], cache8.shape[1], _ptr(block_table), block_table.shape[1],
+             _ptr(seq_lens), B, H, int(max_seq_len), float(softmax_scale), float(kv_scale),
+             _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+             _ptr(dev_status), _stream(stream)]
+    _check(fn(*args))
     return out
 
 

@@ -13,6 +13,9 @@ namespace mla {
 cudaError_t launch_cache_append(const void *kv_new, const int64_t *slots, int64_t num_tokens,
                                 void *cache, int64_t num_slots, int32_t *dev_status,
                                 cudaStream_t stream);
+cudaError_t launch_cache_append_fp8(const void *kv_new, const int64_t *slots, int64_t num_tokens,
+                                    void *cache, int64_t num_slots, float inv_scale,
+                                    int32_t *dev_status, cudaStream_t stream);
 cudaError_t launch_plan(const int32_t *seq_lens, const int32_t *block_table, int64_t num_blocks,
                         int32_t batch, int32_t unit_tokens, int32_t max_blocks_per_seq,
                         int32_t block_size, int32_t max_ranges, void *ws, int32_t heads,
@@ -30,7 +33,7 @@ cudaError_t launch_decode_tc(const void *q, const void *cache, int64_t num_block
                              const int32_t *block_table, int32_t max_blocks_per_seq, int32_t batch,
                              float softmax_scale, void *out, float *lse, void *ws,
                              int32_t max_ranges, int32_t *dev_status, cudaStream_t stream,
-                             const void *kv_new = nullptr);
+                             const void *kv_new = nullptr, bool fp8 = false, float kv_scale = 1.f);
 
 namespace {
 
@@ -79,6 +82,8 @@ mla_status_t need_all_heads(int32_t num_heads) {
     return fail(MLA_ERR_UNSUPPORTED, "num_heads %d: this entry point needs %d", num_heads, kHeads);
   return MLA_OK;
 }
+
+bool kv_scale_ok(float kv_scale) { return std::isfinite(kv_scale) && kv_scale > 0.f; }
 
 bool block_size_ok(int32_t bs) { return bs == 16 || bs == 32 || bs == 64 || bs == 128 || bs == 256; }
 
@@ -349,6 +354,81 @@ mla_status_t mla_combine(const float *o_partial, const float *lse_partial,
   cudaError_t e = launch_offsets_combine(o_partial, lse_partial, split_offsets, batch, num_heads,
                                          out, lse, (cudaStream_t)stream);
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "combine launch");
+}
+
+mla_status_t mla_cache_append_fp8(const void *kv_new, const int64_t *slot_mapping,
+                                  int64_t num_tokens, void *cache8, int64_t num_blocks,
+                                  int32_t block_size, float kv_scale, int32_t *dev_status,
+                                  void *stream) {
+  TraceRange trace_range("mla_cache_append_fp8");
+  g_detail.clear();
+  if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARGUMENT, "num_tokens < 0");
+  if (block_size <= 0) return fail(MLA_ERR_INVALID_ARGUMENT, "block_size %d <= 0", block_size);
+  if (num_blocks <= 0) return fail(MLA_ERR_INVALID_ARGUMENT, "num_blocks <= 0");
+  if (!kv_scale_ok(kv_scale))
+    return fail(MLA_ERR_INVALID_ARGUMENT, "kv_scale must be positive and finite");
+  if (num_tokens == 0) return MLA_OK;
+  if (!kv_new || !slot_mapping || !cache8) return fail(MLA_ERR_INVALID_ARGUMENT, "null pointer");
+  if (!aligned(kv_new, 16) || !aligned(cache8, 16) || !aligned(slot_mapping, 8))
+    return fail(MLA_ERR_INVALID_ARGUMENT,
+                "kv_new/cache8 must be 16-byte, slot_mapping 8-byte aligned");
+  cudaError_t e = launch_cache_append_fp8(kv_new, slot_mapping, num_tokens, cache8,
+                                          num_blocks * (int64_t)block_size, 1.f / kv_scale,
+                                          dev_status, (cudaStream_t)stream);
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_cache_append_fp8 launch");
+}
+
+mla_status_t mla_decode_fp8_planned(const void *q, void *cache8, const void *kv_new,
+                                    int64_t num_blocks, int32_t block_size,
+                                    const int32_t *block_table, int32_t max_blocks_per_seq,
+                                    const int32_t *seq_lens, int32_t batch, int32_t num_heads,
+                                    int32_t max_seq_len, float softmax_scale, float kv_scale,
+                                    void *out, float *lse, void *workspace, size_t workspace_bytes,
+                                    int32_t *dev_status, void *stream) {
+  TraceRange trace_range("mla_decode_fp8_planned");
+  g_detail.clear();
+  if (need_all_heads(num_heads) != MLA_OK) return MLA_ERR_UNSUPPORTED;
+  mla_status_t s = check_decode_args(q, cache8, num_blocks, block_size, block_table,
+                                     max_blocks_per_seq, seq_lens, batch, num_heads, max_seq_len,
+                                     softmax_scale, out, lse, workspace, workspace_bytes);
+  if (s != MLA_OK) return s;
+  if (!kv_scale_ok(kv_scale))
+    return fail(MLA_ERR_INVALID_ARGUMENT, "kv_scale must be positive and finite");
+  if (batch == 0) return MLA_OK;
+  if (kv_new && !aligned(kv_new, 16))
+    return fail(MLA_ERR_INVALID_ARGUMENT, "kv_new must be 16-byte aligned");
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = launch_decode_tc(q, cache8, num_blocks, block_size, block_table,
+                                   max_blocks_per_seq, batch, softmax_scale, out, lse, workspace,
+                                   max_ranges_current(), dev_status, st, kv_new, true, kv_scale);
+  if (e != cudaSuccess) return cuda_fail(e, "FP8 decode launch");
+  e = launch_plan_combine(workspace, batch, num_heads, max_ranges_current(), out, lse, st);
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e, "combine launch");
+}
+
+mla_status_t mla_decode_fp8(const void *q, const void *cache8, int64_t num_blocks,
+                            int32_t block_size, const int32_t *block_table,
+                            int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t batch,
+                            int32_t num_heads, int32_t max_seq_len, float softmax_scale,
+                            float kv_scale, void *out, float *lse, void *workspace,
+                            size_t workspace_bytes, int32_t *dev_status, void *stream) {
+  TraceRange trace_range("mla_decode_fp8");
+  g_detail.clear();
+  if (need_all_heads(num_heads) != MLA_OK) return MLA_ERR_UNSUPPORTED;
+  mla_status_t s = check_decode_args(q, cache8, num_blocks, block_size, block_table,
+                                     max_blocks_per_seq, seq_lens, batch, num_heads, max_seq_len,
+                                     softmax_scale, out, lse, workspace, workspace_bytes);
+  if (s != MLA_OK) return s;
+  if (!kv_scale_ok(kv_scale))
+    return fail(MLA_ERR_INVALID_ARGUMENT, "kv_scale must be positive and finite");
+  if (batch == 0) return MLA_OK;
+  s = mla_decode_plan(seq_lens, block_table, batch, num_heads, max_blocks_per_seq, block_size,
+                      num_blocks, workspace, workspace_bytes, dev_status, stream);
+  if (s != MLA_OK) return s;
+  return mla_decode_fp8_planned(q, const_cast<void *>(cache8), nullptr, num_blocks, block_size,
+                                block_table, max_blocks_per_seq, seq_lens, batch, num_heads,
+                                max_seq_len, softmax_scale, kv_scale, out, lse, workspace,
+                                workspace_bytes, dev_status, stream);
 }
 
 mla_status_t mla_selftest_wait_timeout(uint64_t budget_ns, int32_t *dev_status,

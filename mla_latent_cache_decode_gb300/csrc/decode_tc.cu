@@ -40,10 +40,22 @@
 // warps 4-7 (one thread per head) run the online softmax with lazy rescaling
 // of O and write the output (or split partials plus log-sum-exp); warp 4 owns
 // the tensor memory allocation.
+//
+// FP8 cache (kFp8).  The cache holds one E4M3 byte per element, 576 bytes per
+// token per layer [MLA 的 TP 切分 (10100.com), opening paragraph and section
+// 5.1], with one scale per layer (a code c stands for value(c) * kv_scale).
+// Each part of a tile lands by TMA in the upper half of its 16-bit slot and
+// two more warps (10: the other part, 11: the own part) widen it in place to
+// f16, which holds every E4M3 value exactly; the MMAs then run on f16
+// operands (kind::f16 needs A and B of one type), so each segment's q is also
+// turned into f16 in place once it lands (exact for |q| in [2^-14, 65504],
+// saturating above), and P is packed as f16.  kv_scale leaves the MMAs: the
+// scores use softmax_scale * kv_scale, the output is multiplied by kv_scale.
 #include <atomic>
 #include <mutex>
 
 #include "common.cuh"
+#include "fp8.cuh"
 #include "sm100.cuh"
 
 namespace mla {
@@ -56,7 +68,11 @@ constexpr int kSlots = 2;                  // slots per part
 constexpr int kVHalf = 256;                // output dims per CTA
 constexpr int kChunkBytes = kTile * 128;   // one 64-dim, 64-token SW128 chunk: 8 KB
 constexpr int kQChunkBytes = 128 * 128;    // one 64-dim chunk of Q for 128 heads: 16 KB
-constexpr int kThreads = 320;              // 10 warps
+constexpr int kThreads = 320;              // 10 warps (bf16 cache)
+constexpr int kThreadsFp8 = 384;           // 12 warps: + two FP8 converter warps
+constexpr int kOtherStage = 20 * 1024;     // FP8 staging: upper half of an "other" slot
+constexpr int kOwnStage = 16 * 1024;       // FP8 staging: upper half of an "own" slot
+constexpr int kChunkBytes8 = kTile * 64;   // one 64-dim, 64-token FP8 chunk: 4 KB
 constexpr int kSoftmaxThreads = 128;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;  // S buffers at kColS + 64 * (g & 1)
@@ -84,6 +100,9 @@ struct __align__(1024) Smem {
   uint64_t qk_seq[2];
   uint64_t qown_full, q_full, q_tmem, q_free, fin_qk, fin_pv, row_ready;
   uint64_t stage_free;  // one phase: the staged first Q own dims have been copied
+  // FP8 cache: the TMA of a part landed in its staging half (other/own), and
+  // each segment's q was turned into f16 (own dims + rope / other dims)
+  uint64_t other_staged[kSlots], own_staged[kSlots], qown_conv, q_conv;
   // one phase: every warp is done with its role (all its tensor-memory work,
   // the operations it issued complete)
   uint64_t roles_done;
@@ -123,6 +142,8 @@ struct Params {
   int32_t *dev_status;
   const uint4 *kv_new;  // optional: row b is request b's newest token, stored before decoding
   uint4 *cache_rows;    // the cache, for those stores
+  float kv_scale;       // FP8 cache: the value of a code is value(code) * kv_scale
+  float kv_inv_scale;   // FP8 cache: a new row is stored as code(x * kv_inv_scale)
 };
 
 // Segments of range p, in plan order: request b, tokens [t0, t1), partial
@@ -194,8 +215,56 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// FP8 cache: widen one part of a tile (nch chunks of 64 dims x 64 rows) from
+// its E4M3 staging (chunk c at stage + 4 KB c, row r at + 64 r) to f16 in the
+// 128-byte-swizzled operand layout (chunk c at dst + 8 KB c, row r at + 128 r,
+// 16-byte unit u at ((u ^ (r & 7)) << 4)).  One warp; the staging is the
+// upper half of the same slot, so the warp walks chunks and, in each, rows in
+// groups of eight, reading a group before writing it: a group's writes end at
+// or before the first byte of any staging row still to be read (checked for
+// the last chunk of either part, where the two come closest).
+template <int kNch>
+__device__ __forceinline__ void widen_part_fp8(uint8_t *dst, const uint8_t *stage, int lane) {
+  const int q4 = lane & 3;
+#pragma unroll 1
+  for (int c = 0; c < kNch; ++c) {
+#pragma unroll 2
+    for (int it = 0; it < kTile / 8; ++it) {
+      const int r = it * 8 + (lane >> 2);
+      const uint4 v = *reinterpret_cast<const uint4 *>(stage + c * kChunkBytes8 + r * 64 + q4 * 16);
+      uint4 o0, o1;
+      o0.x = e4m3x2_to_f16x2(v.x); o0.y = e4m3x2_to_f16x2(v.x >> 16);
+      o0.z = e4m3x2_to_f16x2(v.y); o0.w = e4m3x2_to_f16x2(v.y >> 16);
+      o1.x = e4m3x2_to_f16x2(v.z); o1.y = e4m3x2_to_f16x2(v.z >> 16);
+      o1.z = e4m3x2_to_f16x2(v.w); o1.w = e4m3x2_to_f16x2(v.w >> 16);
+      __syncwarp();  // every lane has read its part of the group before any writes
+      uint8_t *row = dst + c * kChunkBytes + r * 128;
+      *reinterpret_cast<uint4 *>(row + (((2 * q4) ^ (r & 7)) << 4)) = o0;
+      *reinterpret_cast<uint4 *>(row + (((2 * q4 + 1) ^ (r & 7)) << 4)) = o1;
+    }
+  }
+}
+
+// FP8 cache: turn bytes of bf16 q in shared memory into f16 in place (the
+// operand layout is the same for both 16-bit types).  One warp.
+__device__ __forceinline__ void q_to_f16(uint8_t *buf, int bytes, int lane) {
+  for (int off = lane * 16; off < bytes; off += 32 * 16) {
+    uint4 w = *reinterpret_cast<const uint4 *>(buf + off);
+    w.x = bf16x2_to_f16x2(w.x); w.y = bf16x2_to_f16x2(w.y);
+    w.z = bf16x2_to_f16x2(w.z); w.w = bf16x2_to_f16x2(w.w);
+    *reinterpret_cast<uint4 *>(buf + off) = w;
+  }
+}
+
+template <bool kFp8>
+__global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
     decode_tc_kernel(const __grid_constant__ Maps maps, const Params prm) {
+  constexpr int kNumThreads = kFp8 ? kThreadsFp8 : kThreads;
   extern __shared__ uint8_t smem_raw[];
   Smem &s = *reinterpret_cast<Smem *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -229,7 +298,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&s.q_free), 2);  // both S issuers
     mbar_init(smem_u32(&s.fin_qk), 2);
     mbar_init(smem_u32(&s.fin_pv), 1);
-    mbar_init(smem_u32(&s.roles_done), kThreads / 32);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(smem_u32(&s.other_staged[i]), 1);
+      mbar_init(smem_u32(&s.own_staged[i]), 1);
+    }
+    mbar_init(smem_u32(&s.qown_conv), 1);
+    mbar_init(smem_u32(&s.q_conv), 1);
+    mbar_init(smem_u32(&s.roles_done), kNumThreads / 32);
     s.abort = 0;
     fence_mbarrier_init_cluster();
   }
@@ -262,7 +337,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int32_t t0, t1, slot_p;
       uint32_t g = 0;
       const int box_rows = BS < kTile ? BS : kTile;
-      const uint32_t box_bytes = (uint32_t)(box_rows * 128);
+      const uint32_t box_bytes = (uint32_t)(box_rows * (kFp8 ? 64 : 128));
+      // where chunk c, page box j of a part lands: its 16-bit slot, or with an
+      // FP8 cache the staging half of that slot
+      auto part_dst = [&](const uint8_t *slot_base, int stage_off, int c, int j) -> uint32_t {
+        return kFp8 ? smem_u32(slot_base) + stage_off + c * kChunkBytes8 + j * box_bytes
+                    : smem_u32(slot_base) + c * kChunkBytes + j * box_bytes;
+      };
       const int64_t nb = prm.num_blocks;
       // Block-table entries of the next tile are loaded one tile ahead into
       // registers: plain loads whose latency overlaps this tile's slot wait.
@@ -339,16 +420,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            const uint32_t bar = smem_u32(&s.own_full[slot]);
+            const uint32_t bar = smem_u32(kFp8 ? &s.own_staged[slot] : &s.own_full[slot]);
             mbar_arrive_expect_tx(bar, 4u * nbx * box_bytes);
             if (big_pages) {
-              tma_load_3d_hint(smem_u32(s.own[slot][0]), &maps.kv4, 0, y[0], own0, bar, policy);
+              tma_load_3d_hint(part_dst(s.own[slot][0], kOwnStage, 0, 0), &maps.kv4, 0, y[0], own0,
+                               bar, policy);
             } else {
 #pragma unroll
               for (int j = 0; j < kTile / 16; ++j) {
                 if (j >= nbx) break;
                 for (int c = 0; c < 4; ++c)
-                  tma_load_2d_hint(smem_u32(s.own[slot][c]) + j * box_bytes, &maps.kv2d,
+                  tma_load_2d_hint(part_dst(s.own[slot][0], kOwnStage, c, j), &maps.kv2d,
                                    64 * (own0 + c), y[j], bar, policy);
               }
             }
@@ -363,21 +445,24 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            const uint32_t bar = smem_u32(&s.other_full[slot]);
+            const uint32_t bar = smem_u32(kFp8 ? &s.other_staged[slot] : &s.other_full[slot]);
             mbar_arrive_expect_tx(bar, 5u * nbx * box_bytes);
             if (big_pages) {
               if (half == 0) {  // other = chunks 4..7, rope = chunk 8: contiguous
-                tma_load_3d_hint(smem_u32(s.other[slot][0]), &maps.kv5, 0, y[0], 4, bar, policy);
+                tma_load_3d_hint(part_dst(s.other[slot][0], kOtherStage, 0, 0), &maps.kv5, 0, y[0],
+                                 4, bar, policy);
               } else {          // other = chunks 0..3, then rope
-                tma_load_3d_hint(smem_u32(s.other[slot][0]), &maps.kv4, 0, y[0], 0, bar, policy);
-                tma_load_3d_hint(smem_u32(s.other[slot][4]), &maps.kv1, 0, y[0], 8, bar, policy);
+                tma_load_3d_hint(part_dst(s.other[slot][0], kOtherStage, 0, 0), &maps.kv4, 0, y[0],
+                                 0, bar, policy);
+                tma_load_3d_hint(part_dst(s.other[slot][0], kOtherStage, 4, 0), &maps.kv1, 0, y[0],
+                                 8, bar, policy);
               }
             } else {
 #pragma unroll
               for (int j = 0; j < kTile / 16; ++j) {
                 if (j >= nbx) break;
                 for (int c = 0; c < 5; ++c)
-                  tma_load_2d_hint(smem_u32(s.other[slot][c]) + j * box_bytes, &maps.kv2d,
+                  tma_load_2d_hint(part_dst(s.other[slot][0], kOtherStage, c, j), &maps.kv2d,
                                    c < 4 ? 64 * (oth0 + c) : 512, y[j], bar, policy);
               }
             }
@@ -386,9 +471,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (s.abort) {
         // the consumers gave up: let the last issued loads land before exit
-        for (int i = 0; i < kSlots; ++i)
-          (void)mbar_wait(smem_u32(own_role ? &s.own_full[i] : &s.other_full[i]), 0, nullptr,
-                          kDrainBudgetNs);
+        for (int i = 0; i < kSlots; ++i) {
+          uint64_t *landed = kFp8 ? (own_role ? &s.own_staged[i] : &s.other_staged[i])
+                                  : (own_role ? &s.own_full[i] : &s.other_full[i]);
+          (void)mbar_wait(smem_u32(landed), 0, nullptr, kDrainBudgetNs);
+        }
       }
     }
   } else if (warp == 1 || warp == 8) {
@@ -406,7 +493,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       it.init(v, prm.batch, pair, seg_n, seg_first);
       int32_t t0, t1, slot_p;
       uint32_t g = 0, seg = 0;
-      const uint32_t id = idesc_bf16_f32(128, kTile, 0);
+      const uint32_t id = kFp8 ? idesc_f16_f32(128, kTile, 0) : idesc_bf16_f32(128, kTile, 0);
+      // Q in place: its TMA with a bf16 cache, its conversion to f16 with FP8
+      uint64_t *qown_ready = kFp8 ? &s.qown_conv : &s.qown_full;
+      uint64_t *qoth_ready = kFp8 ? &s.q_conv : &s.q_full;
       // descriptors of slot 0 / chunk 0; chunks, slots and k-steps add their
       // byte offset >> 4 to the 14-bit start-address field (no carry: every
       // shared-memory address here is below 2^18)
@@ -417,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t a_q = tmem + kColQ;
       bool ok = true;
       while (ok && it.next(t0, t1, slot_p)) {
-        if (!mbar_wait(smem_u32(&s.qown_full), seg & 1u, abort_flag, kWaitBudgetNs)) {
+        if (!mbar_wait(smem_u32(qown_ready), seg & 1u, abort_flag, kWaitBudgetNs)) {
           set_abort(s, prm.dev_status);
           break;
         }
@@ -439,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (seg == 0) mma_commit(smem_u32(&s.stage_free));
         }
         if (!mbar_wait(smem_u32(&s.q_tmem), seg & 1u, abort_flag, kWaitBudgetNs) ||
-            !mbar_wait(smem_u32(&s.q_full), seg & 1u, abort_flag, kWaitBudgetNs)) {
+            !mbar_wait(smem_u32(qoth_ready), seg & 1u, abort_flag, kWaitBudgetNs)) {
           set_abort(s, prm.dev_status);
           break;
         }
@@ -518,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       it.init(v, prm.batch, pair, seg_n, seg_first);
       int32_t t0, t1, slot_p;
       uint32_t g = 0;
-      const uint32_t id_pv = idesc_bf16_f32(128, kVHalf, 1);
+      const uint32_t id_pv = kFp8 ? idesc_f16_f32(128, kVHalf, 1) : idesc_bf16_f32(128, kVHalf, 1);
       const uint64_t d_own = smem_desc(smem_u32(s.own[0][0]), kChunkBytes, 1024, kSwizzle128B);
       bool ok = true;
       while (ok && it.next(t0, t1, slot_p)) {
@@ -616,8 +706,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int64_t row = (int64_t)blk * BS + pos % BS;
           const uint4 *src = prm.kv_new + (int64_t)it.b * (kRow / 8);
-          uint4 *dst = prm.cache_rows + row * (kRow / 8);
-          for (int k = lane; k < kRow / 8; k += 32) dst[k] = __ldg(src + k);
+          if (kFp8) {  // 8 elements (16 bytes of bf16) -> 8 codes per word
+            uint2 *dst = reinterpret_cast<uint2 *>(prm.cache_rows) + row * (kRow / 8);
+            for (int k = lane; k < kRow / 8; k += 32)
+              dst[k] = quantize_bf16x8(__ldg(src + k), prm.kv_inv_scale);
+          } else {
+            uint4 *dst = prm.cache_rows + row * (kRow / 8);
+            for (int k = lane; k < kRow / 8; k += 32) dst[k] = __ldg(src + k);
+          }
         }
         fence_proxy_async_global();
         __syncwarp();
@@ -629,6 +725,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (s.abort) {  // let the last issued loads land before exit
           (void)mbar_wait(smem_u32(&s.qown_full), 0, nullptr, kDrainBudgetNs);
           (void)mbar_wait(smem_u32(&s.q_full), 0, nullptr, kDrainBudgetNs);
+        }
+      }
+    }
+  } else if (kFp8 && (warp == 10 || warp == 11)) {
+    // ------------------------------------------------------------ FP8 converters
+    // Warp 10 widens every tile's other part, warp 11 its own part, in tile
+    // order, each from the staging half of the slot, and hands the slot to
+    // the MMAs (other_full / own_full).  Before a segment's first tile, warp
+    // 11 turns that segment's q own dims and rope into f16 (qown_conv), warp 10
+    // its other dims (q_conv), so that every MMA operand is f16.
+    if (active) {
+      const bool own_part = (warp == 11);
+      SegIter it;
+      it.init(v, prm.batch, pair, seg_n, seg_first);
+      int32_t t0, t1, slot_p;
+      uint32_t g = 0, seg = 0;
+      bool ok = true;
+      while (ok && it.next(t0, t1, slot_p)) {
+        if (own_part) {
+          if (!warp_wait(smem_u32(&s.qown_full), seg & 1u, abort_flag)) {
+            if (lane == 0) set_abort(s, prm.dev_status);
+            break;
+          }
+          for (int c = 0; c < 4; ++c)
+            q_to_f16(seg == 0 ? q_stage_chunk(s, c) : s.q_other[c], kQChunkBytes, lane);
+          q_to_f16(s.q_rope, kQChunkBytes, lane);
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&s.qown_conv));
+        } else {
+          if (!warp_wait(smem_u32(&s.q_full), seg & 1u, abort_flag)) {
+            if (lane == 0) set_abort(s, prm.dev_status);
+            break;
+          }
+          for (int c = 0; c < 4; ++c) q_to_f16(s.q_other[c], kQChunkBytes, lane);
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&s.q_conv));
+        }
+        ++seg;
+        for (int32_t tt = t0; tt < t1; tt += kTile, ++g) {
+          const int slot = g % kSlots;
+          const uint32_t ph = (g / kSlots) & 1u;
+          if (!warp_wait(smem_u32(own_part ? &s.own_staged[slot] : &s.other_staged[slot]), ph,
+                         abort_flag)) {
+            if (lane == 0) set_abort(s, prm.dev_status);
+            ok = false;
+            break;
+          }
+          if (own_part)
+            widen_part_fp8<4>(s.own[slot][0], s.own[slot][0] + kOwnStage, lane);
+          else
+            widen_part_fp8<5>(s.other[slot][0], s.other[slot][0] + kOtherStage, lane);
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(own_part ? &s.own_full[slot] : &s.other_full[slot]));
         }
       }
     }
@@ -717,7 +869,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < kTile; k += 2) {
             const float p0 = ex2_approx(fmaf(x[k], c, nm)), p1 = ex2_approx(fmaf(x[k + 1], c, nm));
             ps[(k >> 1) & 7] += p0 + p1;
-            pk[k / 2] = pack_bf16(p0, p1);
+            pk[k / 2] = kFp8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
           }
           const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
           l = l * alpha + psum;
@@ -767,7 +919,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const float inv = 1.f / l;
+        // with an FP8 cache every value row carries the layer's kv_scale
+        const float inv = kFp8 ? prm.kv_scale / l : 1.f / l;
         const float lse_val = (m_used + log2f(l)) * 0.69314718055994531f;
         if (slot_p < 0) {
           uint4 *dst = (uint4 *)(prm.out + ((int64_t)b * kHeads + h) * kVDim + half * kVHalf);
@@ -928,6 +1081,34 @@ bool encode_3d(CUtensorMap *m, const void *base, int64_t rows, uint32_t box_rows
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+// FP8 cache [rows x 576] bytes (row stride 576 B), unswizzled: a box
+// {64 bytes, box_rows} lands as box_rows rows of 64 bytes.
+bool encode_2d_u8(CUtensorMap *m, const void *base, int64_t rows, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)kRow, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kRow};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The FP8 rows viewed as {64 bytes, rows, 9 chunks of 64 bytes}: a box
+// {64, box_rows, chunks} lands chunk after chunk, each box_rows x 64 bytes.
+bool encode_3d_u8(CUtensorMap *m, const void *base, int64_t rows, uint32_t box_rows,
+                  uint32_t chunks) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(kRow / 64)};
+  cuuint64_t strides[2] = {(cuuint64_t)kRow, 64};
+  cuuint32_t box[3] = {64, box_rows, chunks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 }  // namespace
 
 int tc_unit_tokens() { return tc::kTile; }
@@ -952,6 +1133,7 @@ namespace {
 // Eager callers then pay no encode per call; graph replays never did.
 struct KvEntry {
   bool valid;
+  bool fp8;
   int dev;
   const void *base;
   int64_t rows;
@@ -975,16 +1157,26 @@ size_t slot_of_ptr(const void *p) {
   return (size_t)((x >> 8) ^ (x >> 20) ^ (x >> 32)) % kMapCacheSize;
 }
 
-bool kv_maps(int dev, const void *cache, int64_t rows, int32_t block_size, tc::Maps *m) {
+bool kv_maps(int dev, const void *cache, int64_t rows, int32_t block_size, bool fp8,
+             tc::Maps *m) {
   std::lock_guard<std::mutex> lock(g_map_mu);
   KvEntry &e = g_kv_maps[slot_of_ptr(cache)];
-  if (!(e.valid && e.dev == dev && e.base == cache && e.rows == rows && e.block_size == block_size)) {
+  if (!(e.valid && e.dev == dev && e.base == cache && e.rows == rows &&
+        e.block_size == block_size && e.fp8 == fp8)) {
     const uint32_t box_rows = block_size < tc::kTile ? (uint32_t)block_size : (uint32_t)tc::kTile;
     e.valid = false;
-    if (!encode_2d(&e.kv2d, cache, rows, box_rows) || !encode_3d(&e.kv5, cache, rows, box_rows, 5) ||
-        !encode_3d(&e.kv4, cache, rows, box_rows, 4) || !encode_3d(&e.kv1, cache, rows, box_rows, 1))
-      return false;
+    const bool ok =
+        fp8 ? encode_2d_u8(&e.kv2d, cache, rows, box_rows) &&
+                  encode_3d_u8(&e.kv5, cache, rows, box_rows, 5) &&
+                  encode_3d_u8(&e.kv4, cache, rows, box_rows, 4) &&
+                  encode_3d_u8(&e.kv1, cache, rows, box_rows, 1)
+            : encode_2d(&e.kv2d, cache, rows, box_rows) &&
+                  encode_3d(&e.kv5, cache, rows, box_rows, 5) &&
+                  encode_3d(&e.kv4, cache, rows, box_rows, 4) &&
+                  encode_3d(&e.kv1, cache, rows, box_rows, 1);
+    if (!ok) return false;
     e.valid = true;
+    e.fp8 = fp8;
     e.dev = dev;
     e.base = cache;
     e.rows = rows;
@@ -1012,11 +1204,12 @@ bool q_map(int dev, const void *q, int32_t batch, tc::Maps *m) {
   return true;
 }
 
-// the kernel's dynamic shared memory opt-in, set once per device
+// the kernel's dynamic shared memory opt-in, set once per device and cache type
+template <bool kFp8>
 cudaError_t ensure_smem_attr(int dev, size_t smem) {
   static std::atomic<bool> done[64];
   if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute(tc::decode_tc_kernel,
+  const cudaError_t e = cudaFuncSetAttribute(tc::decode_tc_kernel<kFp8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
   return e;
@@ -1027,16 +1220,16 @@ cudaError_t launch_decode_tc(const void *q, const void *cache, int64_t num_block
                              const int32_t *block_table, int32_t max_blocks_per_seq, int32_t batch,
                              float softmax_scale, void *out, float *lse, void *ws,
                              int32_t max_ranges, int32_t *dev_status, cudaStream_t stream,
-                             const void *kv_new) {
+                             const void *kv_new, bool fp8, float kv_scale) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   tc::Maps maps;
-  if (!kv_maps(dev, cache, num_blocks * (int64_t)block_size, block_size, &maps) ||
+  if (!kv_maps(dev, cache, num_blocks * (int64_t)block_size, block_size, fp8, &maps) ||
       !q_map(dev, q, batch, &maps))
     return cudaErrorInvalidValue;
   const size_t smem = sizeof(tc::Smem) + 1024;
-  e = ensure_smem_attr(dev, smem);
+  e = fp8 ? ensure_smem_attr<true>(dev, smem) : ensure_smem_attr<false>(dev, smem);
   if (e != cudaSuccess) return e;
   tc::Params p;
   p.q = (const __nv_bfloat16 *)q;
@@ -1045,7 +1238,11 @@ cudaError_t launch_decode_tc(const void *q, const void *cache, int64_t num_block
   p.block_size = block_size;
   p.num_blocks = (int32_t)num_blocks;
   p.batch = batch;
-  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  // with an FP8 cache the layer's kv_scale multiplies every score
+  p.scale_log2 = fp8 ? softmax_scale * kv_scale * 1.4426950408889634f
+                     : softmax_scale * 1.4426950408889634f;
+  p.kv_scale = fp8 ? kv_scale : 1.f;
+  p.kv_inv_scale = fp8 ? 1.f / kv_scale : 1.f;
   p.out = (__nv_bfloat16 *)out;
   p.lse = lse;
   p.ws = ws;
@@ -1053,7 +1250,10 @@ cudaError_t launch_decode_tc(const void *q, const void *cache, int64_t num_block
   p.dev_status = dev_status;
   p.kv_new = (const uint4 *)kv_new;
   p.cache_rows = (uint4 *)const_cast<void *>(cache);
-  tc::decode_tc_kernel<<<2 * max_ranges, tc::kThreads, smem, stream>>>(maps, p);
+  if (fp8)
+    tc::decode_tc_kernel<true><<<2 * max_ranges, tc::kThreadsFp8, smem, stream>>>(maps, p);
+  else
+    tc::decode_tc_kernel<false><<<2 * max_ranges, tc::kThreads, smem, stream>>>(maps, p);
   return cudaGetLastError();
 }
 

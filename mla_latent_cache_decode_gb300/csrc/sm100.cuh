@@ -266,6 +266,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn_maj
          | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
+// The same with f16 A and B (format code 0).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int b_mn_major) {
+  return (1u << 4)                       // D format: f32
+         | ((uint32_t)b_mn_major << 16)  // B major-ness
+         | ((uint32_t)(N >> 3) << 17)    // N / 8
+         | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
 enum : uint32_t { kSwizzleNone = 0, kSwizzle128B = 2, kSwizzle64B = 4, kSwizzle32B = 6 };
 
 // Shared-memory matrix descriptor (tcgen05 format, version 1).
