@@ -485,6 +485,8 @@ def run_mine(args, w, rank, world, local_rank):
         result["absorption"] = measure_absorption(w, device, stream, hbm_peak)
     if not args.no_tp_compare and world == 1 and w.name.startswith("dp_rank"):
         result["tp_rank"] = measure_tp_rank(device, stream, hbm_peak, ms_step, L)
+    if not args.no_fp8 and world == 1:
+        result["fp8"] = measure_fp8(w, device, stream, hbm_peak, tf_peak, ms_step)
     if not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, W, budget_s=args.cpu_budget)
     if world > 1:
@@ -606,6 +608,80 @@ def measure_tp_rank(device, stream, hbm_peak, dp_ms_step, layers, distinct=4, re
                       f"cycled"}
 
 
+def measure_fp8(w, device, stream, hbm_peak, tf_peak, bf16_ms_step, reps=20):
+    """The same step with an FP8 (E4M3) cache: each of the workload's layers
+    has its own cache of one byte per latent element (576 bytes per token per
+    layer), and the step is one plan, then per layer the fused quantising
+    append + decode and the split combine, in a CUDA graph.  Reported beside
+    the bf16 step, not part of the line's value."""
+    import torch
+    import mla_latent_cache_decode_gb300 as mla
+    bt = mi.make_block_table(mi.rng_for(w.config_id, 0, 1), w.seq_lens, w.block_size,
+                             w.num_blocks())
+    layers = [mi.make_device_layer_fp8(w, l, device, block_table=bt) for l in range(w.layers)]
+    L, B = w.layers, w.batch
+    ws = mla.make_workspace(B, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    outs = [torch.empty((B, 128, 512), dtype=torch.bfloat16, device=device) for _ in range(L)]
+    lses = [torch.empty((B, 128), dtype=torch.float32, device=device) for _ in range(L)]
+    sh = stream.cuda_stream
+    kv_scale = 1.0
+
+    def step():
+        d0 = layers[0]
+        mla.mla_decode_plan(d0["seq_lens"], d0["block_table"], w.block_size, ws,
+                            dev_status=status, stream=sh, num_blocks=w.num_blocks())
+        for l, d in enumerate(layers):
+            mla.mla_decode_fp8_planned(d["q"], d["cache8"], d["block_table"], d["seq_lens"],
+                                       d["softmax_scale"], outs[l], lses[l], kv_scale=kv_scale,
+                                       workspace=ws, dev_status=status, stream=sh,
+                                       kv_new=d["kv_new"] if w.append else None)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"fp8 device status {int(status.item())}"
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    graph.replay()
+    torch.cuda.synchronize()
+    cache_bytes = sum(w.seq_lens) * mi.ROW * L               # one byte per element
+    l2_bytes = torch.cuda.get_device_properties(device).L2_cache_size
+    flush_buf = (torch.empty(2 * l2_bytes, dtype=torch.uint8, device=device)
+                 if cache_bytes < 8 * l2_bytes else None)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for a, b in ev:
+        if flush_buf is not None:
+            with torch.cuda.stream(stream):
+                flush_buf.fill_(0x5A)
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"fp8 device status {int(status.item())}"
+    per = [a.elapsed_time(b) for a, b in ev]
+    ms = statistics.mean(per)
+    step_bytes = (sum(w.seq_lens) * mi.ROW + B * 128 * mi.ROW * 2 + B * 128 * 512 * 2 +
+                  (B * mi.ROW if w.append else 0)) * L
+    flops = algorithmic_flops_per_layer(w) * L
+    roof_us = max(step_bytes / (hbm_peak * 1e9), flops / (tf_peak * 1e12)) * 1e6
+    return {"what": "the same step over an FP8 (E4M3) cache, fused quantising append, "
+                    "CUDA graph; not part of the line's value",
+            "ms_per_step": round(ms, 4), "step_ms_median": round(statistics.median(per), 4),
+            "cache_gb_per_step": round(cache_bytes / 1e9, 4),
+            "cache_gbs": round(cache_bytes / (ms * 1e-3) / 1e9, 1),
+            "frac_of_hbm_peak": round(cache_bytes / (ms * 1e-3) / 1e9 / hbm_peak, 4),
+            "roofline_us": round(roof_us, 1),
+            "roofline_bound": "tensor" if flops / (tf_peak * 1e12) > step_bytes / (hbm_peak * 1e9)
+            else "hbm",
+            "step_roofline_frac": round(roof_us / (ms * 1e3), 4),
+            "vs_bf16_step": round(ms / bf16_ms_step, 3), "kv_scale": kv_scale,
+            "l2": "flushed between timed steps" if flush_buf is not None else "inputs larger than L2"}
+
+
 # ----------------------------------------------------------------------------- oracle on the host
 
 def _host_layer_for_oracle(w, d, bt):
@@ -697,6 +773,8 @@ def main():
                     help="skip the separate timing of the absorption GEMMs")
     ap.add_argument("--no-tp-compare", action="store_true",
                     help="skip timing one TP=8 rank's step over the same node batch (16 heads)")
+    ap.add_argument("--no-fp8", action="store_true",
+                    help="skip timing the same step over an FP8 (E4M3) cache")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--layers", type=int, default=0,
                     help="run only the first N layers of the workload (for profiling captures)")

@@ -223,41 +223,55 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
 // FP8 cache: widen one part of a tile (nch chunks of 64 dims x 64 rows) from
 // its E4M3 staging (chunk c at stage + 4 KB c, row r at + 64 r) to f16 in the
 // 128-byte-swizzled operand layout (chunk c at dst + 8 KB c, row r at + 128 r,
-// 16-byte unit u at ((u ^ (r & 7)) << 4)).  One warp; the staging is the
-// upper half of the same slot, so the warp walks chunks and, in each, rows in
-// groups of eight, reading a group before writing it: a group's writes end at
-// or before the first byte of any staging row still to be read (checked for
-// the last chunk of either part, where the two come closest).
+// 16-byte unit u at ((u ^ (r & 7)) << 4)).  One warp, a chunk at a time: lane
+// l reads 16 staging bytes of rows l/4, l/4 + 8, ..., all eight loads in
+// flight, converts them, and writes them only after the whole warp has read
+// the chunk.  The staging is the upper half of the same slot; a chunk's
+// writes end at or before the first staging byte of the next chunk (for
+// every chunk of either part: 8 KB (c + 1) <= stage offset + 4 KB (c + 1)).
 template <int kNch>
 __device__ __forceinline__ void widen_part_fp8(uint8_t *dst, const uint8_t *stage, int lane) {
-  const int q4 = lane & 3;
+  const int q4 = lane & 3, r0 = lane >> 2;
 #pragma unroll 1
   for (int c = 0; c < kNch; ++c) {
-#pragma unroll 2
+    uint4 v[kTile / 8];
+#pragma unroll
+    for (int it = 0; it < kTile / 8; ++it)
+      v[it] = *reinterpret_cast<const uint4 *>(stage + c * kChunkBytes8 + (it * 8 + r0) * 64 +
+                                               q4 * 16);
+    __syncwarp();  // the whole chunk is read before any of it is overwritten
+#pragma unroll
     for (int it = 0; it < kTile / 8; ++it) {
-      const int r = it * 8 + (lane >> 2);
-      const uint4 v = *reinterpret_cast<const uint4 *>(stage + c * kChunkBytes8 + r * 64 + q4 * 16);
+      const int r = it * 8 + r0;
       uint4 o0, o1;
-      o0.x = e4m3x2_to_f16x2(v.x); o0.y = e4m3x2_to_f16x2(v.x >> 16);
-      o0.z = e4m3x2_to_f16x2(v.y); o0.w = e4m3x2_to_f16x2(v.y >> 16);
-      o1.x = e4m3x2_to_f16x2(v.z); o1.y = e4m3x2_to_f16x2(v.z >> 16);
-      o1.z = e4m3x2_to_f16x2(v.w); o1.w = e4m3x2_to_f16x2(v.w >> 16);
-      __syncwarp();  // every lane has read its part of the group before any writes
+      o0.x = e4m3x2_to_f16x2(v[it].x); o0.y = e4m3x2_to_f16x2(v[it].x >> 16);
+      o0.z = e4m3x2_to_f16x2(v[it].y); o0.w = e4m3x2_to_f16x2(v[it].y >> 16);
+      o1.x = e4m3x2_to_f16x2(v[it].z); o1.y = e4m3x2_to_f16x2(v[it].z >> 16);
+      o1.z = e4m3x2_to_f16x2(v[it].w); o1.w = e4m3x2_to_f16x2(v[it].w >> 16);
       uint8_t *row = dst + c * kChunkBytes + r * 128;
       *reinterpret_cast<uint4 *>(row + (((2 * q4) ^ (r & 7)) << 4)) = o0;
       *reinterpret_cast<uint4 *>(row + (((2 * q4 + 1) ^ (r & 7)) << 4)) = o1;
     }
+    __syncwarp();
   }
 }
 
 // FP8 cache: turn bytes of bf16 q in shared memory into f16 in place (the
-// operand layout is the same for both 16-bit types).  One warp.
+// operand layout is the same for both 16-bit types).  One warp, eight 16-byte
+// words per lane in flight.
 __device__ __forceinline__ void q_to_f16(uint8_t *buf, int bytes, int lane) {
-  for (int off = lane * 16; off < bytes; off += 32 * 16) {
-    uint4 w = *reinterpret_cast<const uint4 *>(buf + off);
-    w.x = bf16x2_to_f16x2(w.x); w.y = bf16x2_to_f16x2(w.y);
-    w.z = bf16x2_to_f16x2(w.z); w.w = bf16x2_to_f16x2(w.w);
-    *reinterpret_cast<uint4 *>(buf + off) = w;
+  constexpr int kStep = 32 * 16 * 8;
+  for (int base = 0; base < bytes; base += kStep) {
+    uint4 w[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      w[k] = *reinterpret_cast<const uint4 *>(buf + base + (k * 32 + lane) * 16);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      w[k].x = bf16x2_to_f16x2(w[k].x); w[k].y = bf16x2_to_f16x2(w[k].y);
+      w[k].z = bf16x2_to_f16x2(w[k].z); w[k].w = bf16x2_to_f16x2(w[k].w);
+      *reinterpret_cast<uint4 *>(buf + base + (k * 32 + lane) * 16) = w[k];
+    }
   }
 }
 
