@@ -788,10 +788,14 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
             ok = false;
             break;
           }
-          if (own_part)
-            widen_part_fp8<4>(s.own[slot][0], s.own[slot][0] + kOwnStage, lane);
-          else
-            widen_part_fp8<5>(s.other[slot][0], s.other[slot][0] + kOtherStage, lane);
+          // the slot as one byte array: chunks, then (upper half) the staging
+          if (own_part) {
+            uint8_t *slot_bytes = reinterpret_cast<uint8_t *>(s.own[slot]);
+            widen_part_fp8<4>(slot_bytes, slot_bytes + kOwnStage, lane);
+          } else {
+            uint8_t *slot_bytes = reinterpret_cast<uint8_t *>(s.other[slot]);
+            widen_part_fp8<5>(slot_bytes, slot_bytes + kOtherStage, lane);
+          }
           fence_proxy_async_shared();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(own_part ? &s.own_full[slot] : &s.other_full[slot]));
