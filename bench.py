@@ -152,7 +152,8 @@ def algorithmic_bytes_per_layer(w):
 
 KERNEL_SOURCES = ("mla_latent_cache_decode_gb300/csrc/decode_tc.cu",
                   "mla_latent_cache_decode_gb300/csrc/sm100.cuh",
-                  "mla_latent_cache_decode_gb300/csrc/common.cuh")
+                  "mla_latent_cache_decode_gb300/csrc/common.cuh",
+                  "mla_latent_cache_decode_gb300/csrc/fp8.cuh")
 KERNEL_HEADER = "include/mla.h"
 # the header's constants that reach the decode kernel (its declarations,
 # comments, ABI version and the no-allocation entry point's limits do not)
