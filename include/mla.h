@@ -105,7 +105,8 @@ mla_status_t mla_cache_append(const void *kv_new, const int64_t *slot_mapping,
  * mla_decode_workspace_size — bytes of scratch mla_decode needs on the
  * current device for `batch` requests of `num_heads` heads.  The workspace
  * holds the split plan (units of the token partition, per request) and the
- * fp32 partial results of requests that are split across CTAs.
+ * partial results of requests that are split across CTAs (each range's
+ * normalised output in bf16 with its fp32 log-sum-exp).
  */
 size_t mla_decode_workspace_size(int32_t batch, int32_t num_heads);
 
@@ -185,8 +186,9 @@ mla_status_t mla_decode_planned(const void *q, const void *cache, int64_t num_bl
  * mla_decode_planned (and of mla_decode_append_planned), for callers that want
  * to place or time them apart.  mla_decode_partial runs the decode kernel over
  * the plan's token ranges: requests that lie in one range get their out (and
- * lse) written; requests spread over several ranges leave one fp32 partial
- * result per range in the workspace.  With kv_new non-null it first stores
+ * lse) written; requests spread over several ranges leave one partial result
+ * per range in the workspace (its normalised output in bf16 and its fp32
+ * log-sum-exp; the merge accumulates in fp32).  With kv_new non-null it first stores
  * each request's new row as mla_decode_append_planned does (the cache is
  * written then; with kv_new NULL it is only read).  mla_combine_planned then
  * merges the partials into out / lse (requests that were not split are left

@@ -35,8 +35,8 @@ __device__ __forceinline__ void report(int32_t *dev_status, int32_t code) {
 // placed before its units; a target inside a start cost snaps to the
 // request's first unit), then moved the least needed to keep every range
 // non-empty.  A request whose units lie in one range is written directly; a
-// request spanning k ranges leaves k fp32 partials which are merged by
-// log-sum-exp.  Range p holds at most two partial segments (its first and its
+// request spanning k ranges leaves k partials (bf16 outputs with fp32
+// log-sum-exps) which are merged by log-sum-exp in fp32.  Range p holds at most two partial segments (its first and its
 // last), stored in slots 2p and 2p+1: the segment of request b in range p
 // uses slot 2p if R_p >= U_b (the range starts inside or at b) and 2p+1
 // otherwise.
@@ -103,8 +103,10 @@ struct PlanHeader {
 //   SegRec seg_rec[P_max][kSegCache]
 //   ReqSplit req_split[B]
 //   fp32 lse_part[2 * P_max * H]
-//   fp32 o_part[2 * P_max][512 / 4][H][4]   (one partial's heads of four
-//                                            dims are contiguous)
+//   bf16 o_part[2 * P_max][512 / 8][H][8]   (a partial: the segment's output
+//                                            normalised by its own sum, in the
+//                                            output's type; one partial's heads
+//                                            of eight dims are contiguous)
 struct WorkspaceLayout {
   size_t seq_len, unit_prefix, range_start, range_first, cost_prefix, counters, seg_count, seg_rec, req_split, lse_part,
       o_part, total;
@@ -125,7 +127,7 @@ __host__ __device__ inline WorkspaceLayout workspace_layout(int batch, int heads
   w.seg_rec = o;      o = align256(o + sizeof(SegRec) * kSegCache * (size_t)max_ranges);
   w.req_split = o;    o = align256(o + sizeof(ReqSplit) * (size_t)batch);
   w.lse_part = o;     o = align256(o + sizeof(float) * 2 * (size_t)max_ranges * heads);
-  w.o_part = o;       o = align256(o + sizeof(float) * 2 * (size_t)max_ranges * heads * kVDim);
+  w.o_part = o;       o = align256(o + sizeof(__nv_bfloat16) * 2 * (size_t)max_ranges * heads * kVDim);
   w.total = o;
   return w;
 }
@@ -142,7 +144,7 @@ struct PlanView {
   const SegRec *seg_rec;
   const ReqSplit *req_split;
   float *lse_part;
-  float *o_part;
+  __nv_bfloat16 *o_part;
 };
 
 __host__ __device__ inline PlanView plan_view(void *ws, int batch, int heads, int max_ranges) {
@@ -160,7 +162,7 @@ __host__ __device__ inline PlanView plan_view(void *ws, int batch, int heads, in
   v.seg_rec = (const SegRec *)(b + l.seg_rec);
   v.req_split = (const ReqSplit *)(b + l.req_split);
   v.lse_part = (float *)(b + l.lse_part);
-  v.o_part = (float *)(b + l.o_part);
+  v.o_part = (__nv_bfloat16 *)(b + l.o_part);
   return v;
 }
 

@@ -957,22 +957,25 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
           }
           if (prm.lse && half == 0) prm.lse[(int64_t)b * kHeads + h] = lse_val;
         } else {
-          // partials are stored as [slot][dim / 4][head][4]: a warp's 32 heads
-          // of four dims are 512 contiguous bytes, so every float4 store
-          // coalesces (head-major rows, one per thread, cost a line per lane)
+          // partials are stored in bf16 as [slot][dim / 8][head][8]: a warp's
+          // 32 heads of eight dims are 512 contiguous bytes, so every 16-byte
+          // store coalesces (head-major rows, one per thread, cost a line per
+          // lane)
           const int slot = slot_p;
-          float4 *dst = reinterpret_cast<float4 *>(v.o_part) +
-                        ((int64_t)slot * (kVDim / 4) + half * (kVHalf / 4)) * kHeads + h;
+          uint4 *dst = reinterpret_cast<uint4 *>(v.o_part) +
+                       ((int64_t)slot * (kVDim / 8) + half * (kVHalf / 8)) * kHeads + h;
 #pragma unroll 1
           for (int c = 0; c < kVHalf; c += 32) {
             uint32_t o[32];
             tmem_ld32(lane_addr + kColO + c, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              dst[(int64_t)(c / 4 + k) * kHeads] = make_float4(
-                  __uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
-                  __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
+            for (int k = 0; k < 4; ++k)
+              dst[(int64_t)(c / 8 + k) * kHeads] = make_uint4(
+                  pack_bf16(__uint_as_float(o[8 * k]) * inv, __uint_as_float(o[8 * k + 1]) * inv),
+                  pack_bf16(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv),
+                  pack_bf16(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv),
+                  pack_bf16(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv));
           }
           if (half == 0) v.lse_part[(int64_t)slot * kHeads + h] = lse_val;
         }

@@ -299,11 +299,11 @@ __device__ __forceinline__ void combine_row(const float *__restrict__ o_part,
 }
 
 // Merges the partials of every split request of a plan.  The decode stores
-// them as [slot][512 / 4][128][4].  A block takes one request and 16 output
-// dims.  With one split lane (kLanes = 1) its thread h is head h and merges
-// all the request's splits, four at a time with their loads all in flight
-// before any is used (a warp's float4 loads are 512 contiguous bytes of 32
-// heads).  With four split lanes (kLanes = 4; for small batches, whose
+// them in bf16 as [slot][512 / 8][128][8].  A block takes one request and 16
+// output dims.  With one split lane (kLanes = 1) its thread h is head h and
+// merges all the request's splits, four at a time with their loads all in
+// flight before any is used (a warp's 16-byte loads are 512 contiguous bytes
+// of 32 heads), in fp32.  With four split lanes (kLanes = 4; for small batches, whose
 // requests are spread over many ranges) a block takes 32 heads, and warp s
 // merges splits s, s + 4, s + 8, ... of them; the four running results of a
 // head (max, weight sum, 16 weighted dims) are then merged through shared
@@ -344,10 +344,16 @@ __global__ void __launch_bounds__(kHeads) plan_combine_kernel(void *ws, int32_t 
       const int k = k0 + u * kLanes;
       const int64_t w = slot_of_split(k < nsplit ? k : k0);  // k0 < nsplit: a valid slot
       l[u] = k < nsplit ? v.lse_part[w * kHeads + h] : -INFINITY;
-      const float4 *src = reinterpret_cast<const float4 *>(v.o_part) +
-                          (w * (kVDim / 4) + d0 / 4) * kHeads + h;
+      const uint4 *src = reinterpret_cast<const uint4 *>(v.o_part) +
+                         (w * (kVDim / 8) + d0 / 8) * kHeads + h;
 #pragma unroll
-      for (int j = 0; j < kCombDims / 4; ++j) x[u][j] = __ldg(src + (int64_t)j * kHeads);
+      for (int j = 0; j < kCombDims / 8; ++j) {
+        const uint4 raw = __ldg(src + (int64_t)j * kHeads);
+        x[u][2 * j] = make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u),
+                                  __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u));
+        x[u][2 * j + 1] = make_float4(__uint_as_float(raw.z << 16), __uint_as_float(raw.z & 0xffff0000u),
+                                      __uint_as_float(raw.w << 16), __uint_as_float(raw.w & 0xffff0000u));
+      }
     }
     float mc = m;
 #pragma unroll
