@@ -122,7 +122,7 @@ def test_noalloc_without_lse_and_at_an_intermediate_batch():
 def test_maximum_batch_against_oracle():
     """The largest batch the library documents (MLA_NOALLOC_MAX_BATCH = 8192
     requests of 1-24 tokens, page 16): mla_decode with a workspace and
-    mla_decode_noalloc, whose 16 MiB scratch then holds only ~31 of the split
+    mla_decode_noalloc, whose 16 MiB scratch then holds only ~62 of the split
     ranges, both against the oracle on sampled requests and against each
     other everywhere."""
     import mla_latent_cache_decode_gb300 as mla
