@@ -599,7 +599,7 @@ def measure_tp_rank(device, stream, hbm_peak, dp_ms_step, layers, distinct=4, re
     ms = e0.elapsed_time(e1) / reps
     cache_bytes = B * L_tok * mi.ROW * 2 * layers
     return {"what": "one TP=8 rank: the node batch of 159 x 4096 sequences, 16 heads "
-                    "(padded to the kernel's 128), decoded over every layer's full cache",
+                    "(the few-head kernel), decoded over every layer's full cache",
             "heads": heads, "batch": B, "layers": layers, "ms_per_step": round(ms, 3),
             "cache_gb_per_step": round(cache_bytes / 1e9, 3),
             "cache_gbs": round(cache_bytes / (ms * 1e-3) / 1e9, 1),

@@ -274,10 +274,13 @@ def mla_decode_append_planned(q, cache, kv_new, block_table, seq_lens, softmax_s
                    dev_status, stream)
 
 
-def mla_combine_planned(workspace, batch, out, lse=None, num_heads=NUM_HEADS, stream=None):
-    """Merge the partials mla_decode_partial left in `workspace` into out / lse."""
+def mla_combine_planned(workspace, batch, out, lse=None, num_heads=None, stream=None):
+    """Merge the partials mla_decode_partial left in `workspace` into out / lse
+    (num_heads: out's head count unless given)."""
     import torch
     _need(out, torch.bfloat16, 3, "out")
+    if num_heads is None:
+        num_heads = out.shape[1]
     if lse is not None:
         _need(lse, torch.float32, 2, "lse")
     _check(get_lib().mla_combine_planned(_ptr(workspace),

@@ -29,6 +29,15 @@ cudaError_t launch_wait_selftest(int32_t *dev_status, uint64_t budget_ns, uint64
                                  cudaStream_t stream);
 int tc_unit_tokens();
 int tc_max_pairs();
+int tp_max_heads();
+int tp_max_ranges();
+cudaError_t launch_decode_tp(const void *q, const void *cache, int64_t num_blocks,
+                             int32_t block_size, const int32_t *block_table,
+                             int32_t max_blocks_per_seq, int32_t batch, int32_t heads,
+                             float softmax_scale, void *out, float *lse, void *ws,
+                             int32_t max_ranges, int32_t *dev_status, cudaStream_t stream);
+cudaError_t launch_tp_combine(void *ws, int32_t batch, int32_t heads, int32_t max_ranges,
+                              void *out, float *lse, cudaStream_t stream);
 cudaError_t launch_decode_tc(const void *q, const void *cache, int64_t num_blocks, int32_t block_size,
                              const int32_t *block_table, int32_t max_blocks_per_seq, int32_t batch,
                              float softmax_scale, void *out, float *lse, void *ws,
@@ -58,9 +67,12 @@ bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 // Ranges of the plan: one per co-resident CTA pair of the tensor-core kernel.
 int max_ranges_current() { return tc_max_pairs(); }
 
-// Fewer heads than the kernel's 128 (a tensor-parallel rank's share): the
-// workspace holds q padded to 128 heads and the padded output and lse, behind
-// the plan and partials.  The pad heads hold whatever the workspace held:
+// A tensor-parallel rank's few heads (1 to 32) run on their own kernel
+// (decode_tp.cu), whose plan has one range per SM.
+bool few_heads(int32_t num_heads) { return num_heads >= 1 && num_heads <= tp_max_heads(); }
+
+// 33 to 127 heads: the workspace holds q padded to 128 heads and the padded
+// output and lse, behind the plan and partials.  The pad heads hold whatever the workspace held:
 // every head is an independent row of the kernel's work and of the merge, and
 // only the caller's heads are copied out.
 struct Padded {
@@ -75,8 +87,7 @@ Padded padded_layout(int32_t batch) {
   return p;
 }
 
-// mla_decode_partial / mla_combine_planned / mla_decode_append_planned work on
-// the kernel's own 128 heads only
+// The FP8 entry points work on the tensor-core kernel's own 128 heads only
 mla_status_t need_all_heads(int32_t num_heads) {
   if (num_heads != kHeads)
     return fail(MLA_ERR_UNSUPPORTED, "num_heads %d: this entry point needs %d", num_heads, kHeads);
@@ -178,6 +189,10 @@ mla_status_t mla_cache_append(const void *kv_new, const int64_t *slot_mapping, i
 
 size_t mla_decode_workspace_size(int32_t batch, int32_t num_heads) {
   if (batch < 0 || num_heads <= 0 || num_heads > kHeads) return 0;
+  if (few_heads(num_heads)) {
+    const int ranges = tp_max_ranges();
+    return ranges <= 0 ? 0 : workspace_layout(batch, num_heads, ranges).total;
+  }
   const int ranges = max_ranges_current();
   if (ranges <= 0) return 0;
   const size_t plan = workspace_layout(batch, kHeads, ranges).total;
@@ -206,9 +221,11 @@ mla_status_t mla_decode_plan(const int32_t *seq_lens, const int32_t *block_table
     return fail(MLA_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu", workspace_bytes, need);
   if (block_table && num_blocks <= 0)
     return fail(MLA_ERR_INVALID_ARGUMENT, "num_blocks must be > 0 with a block table");
+  const bool few = few_heads(num_heads);
   cudaError_t e = launch_plan(seq_lens, block_table, num_blocks, batch, tc_unit_tokens(),
-                              max_blocks_per_seq, block_size, max_ranges_current(), workspace,
-                              kHeads, dev_status, (cudaStream_t)stream);
+                              max_blocks_per_seq, block_size,
+                              few ? tp_max_ranges() : max_ranges_current(), workspace,
+                              few ? num_heads : kHeads, dev_status, (cudaStream_t)stream);
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "plan launch");
 }
 
@@ -221,13 +238,25 @@ mla_status_t mla_decode_partial(const void *q, void *cache, const void *kv_new,
                                 void *stream) {
   TraceRange trace_range("mla_decode_partial");
   g_detail.clear();
-  if (need_all_heads(num_heads) != MLA_OK) return MLA_ERR_UNSUPPORTED;
+  const bool few = few_heads(num_heads);
+  if (!few && num_heads != kHeads)
+    return fail(MLA_ERR_UNSUPPORTED, "num_heads %d: this entry point takes 1 to %d or %d",
+                num_heads, tp_max_heads(), kHeads);
+  if (few && kv_new)
+    return fail(MLA_ERR_UNSUPPORTED, "the fused append needs %d heads", kHeads);
   mla_status_t s = check_decode_args(q, cache, num_blocks, block_size, block_table,
                                      max_blocks_per_seq, seq_lens, batch, num_heads, max_seq_len,
                                      softmax_scale, out, lse, workspace, workspace_bytes);
   if (s != MLA_OK || batch == 0) return s;
   if (kv_new && !aligned(kv_new, 16))
     return fail(MLA_ERR_INVALID_ARGUMENT, "kv_new must be 16-byte aligned");
+  if (few) {
+    cudaError_t e = launch_decode_tp(q, cache, num_blocks, block_size, block_table,
+                                     max_blocks_per_seq, batch, num_heads, softmax_scale, out,
+                                     lse, workspace, tp_max_ranges(), dev_status,
+                                     (cudaStream_t)stream);
+    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "few-head decode launch");
+  }
   cudaError_t e = launch_decode_tc(q, cache, num_blocks, block_size, block_table,
                                    max_blocks_per_seq, batch, softmax_scale, out, lse, workspace,
                                    max_ranges_current(), dev_status, (cudaStream_t)stream, kv_new);
@@ -259,7 +288,10 @@ mla_status_t mla_combine_planned(void *workspace, size_t workspace_bytes, int32_
   TraceRange trace_range("mla_combine_planned");
   g_detail.clear();
   if (batch < 0) return fail(MLA_ERR_INVALID_ARGUMENT, "batch < 0");
-  if (num_heads != kHeads) return fail(MLA_ERR_UNSUPPORTED, "num_heads must be %d", kHeads);
+  const bool few = few_heads(num_heads);
+  if (!few && num_heads != kHeads)
+    return fail(MLA_ERR_UNSUPPORTED, "num_heads %d: this entry point takes 1 to %d or %d",
+                num_heads, tp_max_heads(), kHeads);
   if (batch == 0) return MLA_OK;
   if (!workspace || !out) return fail(MLA_ERR_INVALID_ARGUMENT, "null pointer");
   if (!aligned(workspace, 256) || !aligned(out, 16) || (lse && !aligned(lse, 4)))
@@ -268,8 +300,11 @@ mla_status_t mla_combine_planned(void *workspace, size_t workspace_bytes, int32_
   if (need == 0) return fail(MLA_ERR_CUDA, "cannot query the current device");
   if (workspace_bytes < need)
     return fail(MLA_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu", workspace_bytes, need);
-  cudaError_t e = launch_plan_combine(workspace, batch, num_heads, max_ranges_current(), out, lse,
-                                      (cudaStream_t)stream);
+  cudaError_t e =
+      few ? launch_tp_combine(workspace, batch, num_heads, tp_max_ranges(), out, lse,
+                              (cudaStream_t)stream)
+          : launch_plan_combine(workspace, batch, num_heads, max_ranges_current(), out, lse,
+                                (cudaStream_t)stream);
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "combine launch");
 }
 
@@ -280,7 +315,7 @@ mla_status_t mla_decode_planned(const void *q, const void *cache, int64_t num_bl
                                 float softmax_scale, void *out, float *lse, void *workspace,
                                 size_t workspace_bytes, int32_t *dev_status, void *stream) {
   TraceRange trace_range("mla_decode_planned");
-  if (num_heads != kHeads) {  // a tensor-parallel rank's heads, padded to 128
+  if (num_heads != kHeads && !few_heads(num_heads)) {  // 33 to 127 heads, padded to 128
     g_detail.clear();
     mla_status_t st = check_decode_args(q, cache, num_blocks, block_size, block_table,
                                         max_blocks_per_seq, seq_lens, batch, num_heads,

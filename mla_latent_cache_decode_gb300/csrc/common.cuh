@@ -166,4 +166,59 @@ __host__ __device__ inline PlanView plan_view(void *ws, int batch, int heads, in
   return v;
 }
 
+// Segments of range p, in plan order: request b, tokens [t0, t1), partial
+// slot (-1: the request is not split).  The first kSegCache come from the
+// plan's records (one memory round trip); later ones, for ranges that cross
+// many short requests, by walking the plan on from the last request.
+// kUnitTokens is the plan's unit (the decode kernels' tile).
+template <int kUnitTokens>
+struct SegIter {
+  PlanView v;
+  int32_t batch, p, n, idx, b;
+  int32_t row0;  // cache row of the current segment's first token, -1 if unknown
+  SegRec first;  // record 0, loaded together with the count
+  // n_ and first_: the range's segment count and first record, loaded by the
+  // caller at kernel entry (one round trip for both, overlapping the setup)
+  __device__ void init(const PlanView &pv, int32_t batch_, int32_t p_, int32_t n_,
+                       const SegRec &first_) {
+    v = pv;
+    batch = batch_;
+    p = p_;
+    n = n_;
+    first = first_;
+    idx = 0;
+    b = -1;
+    row0 = -1;
+  }
+  __device__ bool next(int32_t &t0, int32_t &t1, int32_t &slot) {
+    if (idx >= n) return false;
+    if (idx < kSegCache) {
+      const SegRec r = idx == 0 ? first : v.seg_rec[(int64_t)p * kSegCache + idx];
+      ++idx;
+      b = r.b;
+      t0 = r.t0;
+      t1 = r.t1;
+      slot = r.slot;
+      row0 = r.row0;
+      return true;
+    }
+    row0 = -1;
+    const int32_t r0 = v.range_start[p], r1 = v.range_start[p + 1];
+    for (++b; b < batch; ++b) {
+      const int32_t Ub = v.unit_prefix[b];
+      if (Ub >= r1) return false;
+      const int32_t Ue = v.unit_prefix[b + 1];
+      const int32_t u0 = max(r0, Ub), u1 = min(r1, Ue);
+      if (u0 >= u1) continue;
+      t0 = (u0 - Ub) * kUnitTokens;
+      t1 = min((u1 - Ub) * kUnitTokens, v.seq_len[b]);
+      slot = segment_slot(p, r0, r1, Ub, Ue);
+      ++idx;
+      return true;
+    }
+    return false;
+  }
+};
+
+
 }  // namespace mla

@@ -57,6 +57,7 @@
 #include "common.cuh"
 #include "fp8.cuh"
 #include "sm100.cuh"
+#include "tmap.h"
 
 namespace mla {
 namespace tc {
@@ -144,58 +145,6 @@ struct Params {
   uint4 *cache_rows;    // the cache, for those stores
   float kv_scale;       // FP8 cache: the value of a code is value(code) * kv_scale
   float kv_inv_scale;   // FP8 cache: a new row is stored as code(x * kv_inv_scale)
-};
-
-// Segments of range p, in plan order: request b, tokens [t0, t1), partial
-// slot (-1: the request is not split).  The first kSegCache come from the
-// plan's records (one memory round trip); later ones, for ranges that cross
-// many short requests, by walking the plan on from the last request.
-struct SegIter {
-  PlanView v;
-  int32_t batch, p, n, idx, b;
-  int32_t row0;  // cache row of the current segment's first token, -1 if unknown
-  SegRec first;  // record 0, loaded together with the count
-  // n_ and first_: the range's segment count and first record, loaded by the
-  // caller at kernel entry (one round trip for both, overlapping the setup)
-  __device__ void init(const PlanView &pv, int32_t batch_, int32_t p_, int32_t n_,
-                       const SegRec &first_) {
-    v = pv;
-    batch = batch_;
-    p = p_;
-    n = n_;
-    first = first_;
-    idx = 0;
-    b = -1;
-    row0 = -1;
-  }
-  __device__ bool next(int32_t &t0, int32_t &t1, int32_t &slot) {
-    if (idx >= n) return false;
-    if (idx < kSegCache) {
-      const SegRec r = idx == 0 ? first : v.seg_rec[(int64_t)p * kSegCache + idx];
-      ++idx;
-      b = r.b;
-      t0 = r.t0;
-      t1 = r.t1;
-      slot = r.slot;
-      row0 = r.row0;
-      return true;
-    }
-    row0 = -1;
-    const int32_t r0 = v.range_start[p], r1 = v.range_start[p + 1];
-    for (++b; b < batch; ++b) {
-      const int32_t Ub = v.unit_prefix[b];
-      if (Ub >= r1) return false;
-      const int32_t Ue = v.unit_prefix[b + 1];
-      const int32_t u0 = max(r0, Ub), u1 = min(r1, Ue);
-      if (u0 >= u1) continue;
-      t0 = (u0 - Ub) * kTile;
-      t1 = min((u1 - Ub) * kTile, v.seq_len[b]);
-      slot = segment_slot(p, r0, r1, Ub, Ue);
-      ++idx;
-      return true;
-    }
-    return false;
-  }
 };
 
 __device__ __forceinline__ void set_abort(Smem &s, int32_t *dev_status) {
@@ -346,7 +295,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
       // little later; evict-first lines were often gone by then (ncu: ~19%
       // extra DRAM reads on a 64 x 4096 layer)
       const uint64_t policy = policy_evict_normal();
-      SegIter it;
+      SegIter<kTile> it;
       it.init(v, prm.batch, pair, seg_n, seg_first);
       int32_t t0, t1, slot_p;
       uint32_t g = 0;
@@ -362,7 +311,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
       // Block-table entries of the next tile are loaded one tile ahead into
       // registers: plain loads whose latency overlaps this tile's slot wait.
       // A segment's first tile needs none when the plan's record has its row.
-      SegIter fc = it;  // shares the first record load
+      SegIter<kTile> fc = it;  // shares the first record load
       int32_t fc_t = 0, fc_t1 = 0, fc_slot;
       bool fc_more = true;
       int32_t nxt[kTile / 16];
@@ -503,7 +452,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
     // copies the segment's Q own dims into tensor memory.
     const uint32_t par = warp == 8 ? 1u : 0u;
     if (active && elect_one_sync()) {
-      SegIter it;
+      SegIter<kTile> it;
       it.init(v, prm.batch, pair, seg_n, seg_first);
       int32_t t0, t1, slot_p;
       uint32_t g = 0, seg = 0;
@@ -618,7 +567,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
   } else if (warp == 2) {
     // ------------------------------------------------------------ O += P V issuer
     if (active && elect_one_sync()) {
-      SegIter it;
+      SegIter<kTile> it;
       it.init(v, prm.batch, pair, seg_n, seg_first);
       int32_t t0, t1, slot_p;
       uint32_t g = 0;
@@ -667,7 +616,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
     // usually needed tiles later.
     if (active) {
       const bool leader = elect_one_sync();
-      SegIter qi;
+      SegIter<kTile> qi;
       qi.init(v, prm.batch, pair, seg_n, seg_first);
       int32_t qt0, qt1, qslot;
       uint32_t seg = 0;
@@ -686,7 +635,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
                       64 * (own0 + c), qi.b * kHeads, smem_u32(&s.qown_full));
         tma_load_2d(smem_u32(s.q_rope), &maps.q, 512, qi.b * kHeads, smem_u32(&s.qown_full));
         {  // the next segment's Q rows into L2 meanwhile
-          SegIter nx = qi;
+          SegIter<kTile> nx = qi;
           int32_t a0, a1, aslot;
           if (nx.next(a0, a1, aslot))
             for (int c = 0; c < 9; ++c) tma_prefetch_2d(&maps.q, 64 * c, nx.b * kHeads);
@@ -706,7 +655,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
       if (leader && qi.next(qt0, qt1, qslot)) qok = load_q();
       __syncwarp();
       if (prm.kv_new) {
-        SegIter it;
+        SegIter<kTile> it;
         it.init(v, prm.batch, pair, seg_n, seg_first);
         int32_t t0, t1, slot_p;
         while (it.next(t0, t1, slot_p)) {
@@ -751,7 +700,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
     // its other dims (q_conv), so that every MMA operand is f16.
     if (active) {
       const bool own_part = (warp == 11);
-      SegIter it;
+      SegIter<kTile> it;
       it.init(v, prm.batch, pair, seg_n, seg_first);
       int32_t t0, t1, slot_p;
       uint32_t g = 0, seg = 0;
@@ -819,7 +768,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
     }
 
     if (active) {
-      SegIter it;
+      SegIter<kTile> it;
       it.init(v, prm.batch, pair, seg_n, seg_first);
       int32_t t0, t1, slot_p;
       uint32_t g = 0;  // tiles so far
@@ -827,7 +776,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
       bool have = it.next(t0, t1, slot_p);
       while (ok && have) {
         const int b = it.b;
-        SegIter nx = it;  // the segment after this one, if any
+        SegIter<kTile> nx = it;  // the segment after this one, if any
         int32_t nt0, nt1, nslot;
         const bool have_next = nx.next(nt0, nt1, nslot);
 
@@ -1053,85 +1002,6 @@ cudaError_t launch_wait_selftest(int32_t *dev_status, uint64_t budget_ns, uint64
 
 // ---------------------------------------------------------------------------- host
 
-namespace {
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = (EncodeTiledFn)p;
-  }
-  return fn;
-}
-
-// [rows x 576] bf16 (row stride 1152 B) read in boxes {64 columns, box_rows}.
-bool encode_2d(CUtensorMap *m, const void *base, int64_t rows, uint32_t box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)kRow, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)kRow * 2};
-  cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// The same rows viewed as {64 columns, rows, 9 chunks of 64 columns}: a box
-// {64, box_rows, chunks} lands in shared memory chunk after chunk, each chunk
-// box_rows x 128 B.
-bool encode_3d(CUtensorMap *m, const void *base, int64_t rows, uint32_t box_rows,
-               uint32_t chunks) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(kRow / 64)};
-  cuuint64_t strides[2] = {(cuuint64_t)kRow * 2, 128};
-  cuuint32_t box[3] = {64, box_rows, chunks};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-// FP8 cache [rows x 576] bytes (row stride 576 B), unswizzled: a box
-// {64 bytes, box_rows} lands as box_rows rows of 64 bytes.
-bool encode_2d_u8(CUtensorMap *m, const void *base, int64_t rows, uint32_t box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)kRow, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)kRow};
-  cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// The FP8 rows viewed as {64 bytes, rows, 9 chunks of 64 bytes}: a box
-// {64, box_rows, chunks} lands chunk after chunk, each box_rows x 64 bytes.
-bool encode_3d_u8(CUtensorMap *m, const void *base, int64_t rows, uint32_t box_rows,
-                  uint32_t chunks) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(kRow / 64)};
-  cuuint64_t strides[2] = {(cuuint64_t)kRow, 64};
-  cuuint32_t box[3] = {64, box_rows, chunks};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-}  // namespace
-
 int tc_unit_tokens() { return tc::kTile; }
 
 // Split ranges of the tensor-core kernel: one per pair of SMs (two CTAs of
@@ -1173,28 +1043,24 @@ std::mutex g_map_mu;
 KvEntry g_kv_maps[kMapCacheSize];
 QEntry g_q_maps[kMapCacheSize];
 
-size_t slot_of_ptr(const void *p) {
-  const uint64_t x = (uint64_t)(uintptr_t)p;
-  return (size_t)((x >> 8) ^ (x >> 20) ^ (x >> 32)) % kMapCacheSize;
-}
 
 bool kv_maps(int dev, const void *cache, int64_t rows, int32_t block_size, bool fp8,
              tc::Maps *m) {
   std::lock_guard<std::mutex> lock(g_map_mu);
-  KvEntry &e = g_kv_maps[slot_of_ptr(cache)];
+  KvEntry &e = g_kv_maps[tmap::slot_of_ptr(cache, kMapCacheSize)];
   if (!(e.valid && e.dev == dev && e.base == cache && e.rows == rows &&
         e.block_size == block_size && e.fp8 == fp8)) {
     const uint32_t box_rows = block_size < tc::kTile ? (uint32_t)block_size : (uint32_t)tc::kTile;
     e.valid = false;
     const bool ok =
-        fp8 ? encode_2d_u8(&e.kv2d, cache, rows, box_rows) &&
-                  encode_3d_u8(&e.kv5, cache, rows, box_rows, 5) &&
-                  encode_3d_u8(&e.kv4, cache, rows, box_rows, 4) &&
-                  encode_3d_u8(&e.kv1, cache, rows, box_rows, 1)
-            : encode_2d(&e.kv2d, cache, rows, box_rows) &&
-                  encode_3d(&e.kv5, cache, rows, box_rows, 5) &&
-                  encode_3d(&e.kv4, cache, rows, box_rows, 4) &&
-                  encode_3d(&e.kv1, cache, rows, box_rows, 1);
+        fp8 ? tmap::encode_2d_u8(&e.kv2d, cache, rows, box_rows) &&
+                  tmap::encode_3d_u8(&e.kv5, cache, rows, box_rows, 5) &&
+                  tmap::encode_3d_u8(&e.kv4, cache, rows, box_rows, 4) &&
+                  tmap::encode_3d_u8(&e.kv1, cache, rows, box_rows, 1)
+            : tmap::encode_2d(&e.kv2d, cache, rows, box_rows) &&
+                  tmap::encode_3d(&e.kv5, cache, rows, box_rows, 5) &&
+                  tmap::encode_3d(&e.kv4, cache, rows, box_rows, 4) &&
+                  tmap::encode_3d(&e.kv1, cache, rows, box_rows, 1);
     if (!ok) return false;
     e.valid = true;
     e.fp8 = fp8;
@@ -1212,10 +1078,10 @@ bool kv_maps(int dev, const void *cache, int64_t rows, int32_t block_size, bool 
 
 bool q_map(int dev, const void *q, int32_t batch, tc::Maps *m) {
   std::lock_guard<std::mutex> lock(g_map_mu);
-  QEntry &e = g_q_maps[slot_of_ptr(q)];
+  QEntry &e = g_q_maps[tmap::slot_of_ptr(q, kMapCacheSize)];
   if (!(e.valid && e.dev == dev && e.base == q && e.batch == batch)) {
     e.valid = false;
-    if (!encode_2d(&e.q, q, (int64_t)batch * kHeads, kHeads)) return false;
+    if (!tmap::encode_2d(&e.q, q, (int64_t)batch * kHeads, kHeads)) return false;
     e.valid = true;
     e.dev = dev;
     e.base = q;

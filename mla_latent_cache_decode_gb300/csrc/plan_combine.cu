@@ -451,6 +451,77 @@ cudaError_t launch_plan_combine(void *ws, int32_t batch, int32_t heads, int32_t 
   return cudaGetLastError();
 }
 
+// Merges the partials of the few-head kernel (decode_tp.cu), stored in bf16
+// as [slot][head][512] with fp32 log-sum-exps [slot][head].  A block of 64
+// threads takes one (request, head); thread t merges dims [8 t, 8 t + 8) over
+// all the request's splits, four at a time with their loads in flight, in
+// fp32.  grid = (batch, heads).
+constexpr int kTpCombThreads = kVDim / 8;  // 64
+
+__global__ void __launch_bounds__(kTpCombThreads) tp_combine_kernel(void *ws, int32_t batch,
+                                                                    int32_t heads,
+                                                                    int32_t max_ranges,
+                                                                    __nv_bfloat16 *__restrict__ out,
+                                                                    float *__restrict__ lse) {
+  PlanView v = plan_view(ws, batch, heads, max_ranges);
+  const int b = blockIdx.x, h = blockIdx.y, t = threadIdx.x;
+  const ReqSplit rs = v.req_split[b];
+  if (rs.p0 == rs.p1) return;  // not split (or empty): the decode wrote it
+  const int nsplit = rs.p1 - rs.p0 + 1;
+  auto slot_of_split = [&](int k) -> int64_t {
+    return k == 0 ? 2 * rs.p0 + rs.first_odd : 2 * (rs.p0 + k);
+  };
+  float m = -INFINITY;
+  for (int k = 0; k < nsplit; ++k) m = fmaxf(m, v.lse_part[slot_of_split(k) * heads + h]);
+  float acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+  float z = 0.f;
+  if (m != -INFINITY) {
+    for (int k0 = 0; k0 < nsplit; k0 += kCombGroup) {
+      float l[kCombGroup];
+      uint4 raw[kCombGroup];
+#pragma unroll
+      for (int u = 0; u < kCombGroup; ++u) {
+        const int k = k0 + u;
+        const int64_t w = slot_of_split(k < nsplit ? k : k0);
+        l[u] = k < nsplit ? v.lse_part[w * heads + h] : -INFINITY;
+        raw[u] = __ldg(reinterpret_cast<const uint4 *>(v.o_part + (w * heads + h) * kVDim) + t);
+      }
+#pragma unroll
+      for (int u = 0; u < kCombGroup; ++u) {
+        const float a = l[u] == -INFINITY ? 0.f : __expf(l[u] - m);
+        z += a;
+        const uint32_t w4[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[2 * j] += a * __uint_as_float(w4[j] << 16);
+          acc[2 * j + 1] += a * __uint_as_float(w4[j] & 0xffff0000u);
+        }
+      }
+    }
+  }
+  const float inv = z > 0.f ? 1.f / z : 0.f;
+  uint4 o;
+  uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    __nv_bfloat162 pr = __floats2bfloat162_rn(acc[2 * j] * inv, acc[2 * j + 1] * inv);
+    ow[j] = *reinterpret_cast<uint32_t *>(&pr);
+  }
+  reinterpret_cast<uint4 *>(out + ((int64_t)b * heads + h) * kVDim)[t] = o;
+  if (lse && t == 0) lse[(int64_t)b * heads + h] = z > 0.f ? m + logf(z) : -INFINITY;
+}
+
+cudaError_t launch_tp_combine(void *ws, int32_t batch, int32_t heads, int32_t max_ranges,
+                              void *out, float *lse, cudaStream_t stream) {
+  if (heads < 1 || heads > 65535) return cudaErrorInvalidValue;
+  dim3 grid(batch, heads);
+  tp_combine_kernel<<<grid, kTpCombThreads, 0, stream>>>(ws, batch, heads, max_ranges,
+                                                         (__nv_bfloat16 *)out, lse);
+  return cudaGetLastError();
+}
+
 // The public combine over caller-given split offsets.  grid = (batch, heads).
 __global__ void __launch_bounds__(kCombineThreads) offsets_combine_kernel(
     const float *__restrict__ o_part, const float *__restrict__ lse_part,

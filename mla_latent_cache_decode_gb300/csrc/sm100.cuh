@@ -108,6 +108,16 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// 3-D tiled load of box {x, y, z} into shared memory.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *m, int32_t x,
+                                            int32_t y, int32_t z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
 // 3-D tiled load of box {x, y, z} into shared memory (L2 cache hint).
 __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap *m, int32_t x,
                                                  int32_t y, int32_t z, uint32_t bar,
@@ -243,6 +253,33 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r) {
       : "memory");
 }
 
+// 16-column forms of the two above.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
+// Barrier among `count` threads (a multiple of 32) of the CTA, by id (0 is
+// the one __syncthreads uses).
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ------------------------------------------------------------------ math
 
 // 2^x by the SFU's approximate exponential (PTX ex2.approx.ftz.f32; relative
@@ -255,12 +292,14 @@ __device__ __forceinline__ float ex2_approx(float x) {
 
 // ------------------------------------------------------------------ descriptors
 
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B,
-// A K-major, B K-major (b_mn_major = 0) or MN-major (1), shape M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn_major) {
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, each
+// K-major (0) or MN-major (1), shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn_major,
+                                                      int a_mn_major = 0) {
   return (1u << 4)                       // D format: f32
          | (1u << 7)                     // A format: bf16
          | (1u << 10)                    // B format: bf16
+         | ((uint32_t)a_mn_major << 15)  // A major-ness
          | ((uint32_t)b_mn_major << 16)  // B major-ness
          | ((uint32_t)(N >> 3) << 17)    // N / 8
          | ((uint32_t)(M >> 4) << 24);   // M / 16

@@ -109,17 +109,26 @@ def test_absorption_host_validation(lib):
     assert lib.mla_absorb_out(None, None, 4, 100, None, None, None) == 2
 
 
-def test_partial_entry_points_need_all_heads(lib):
+def test_partial_entry_points_take_few_or_all_heads(lib):
     P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
     lib.mla_decode_partial.argtypes = [P, P, P, i64, i32, P, i32, P, i32, i32, i32, f32, P, P, P,
                                        sz, P, P]
     lib.mla_decode_partial.restype = ctypes.c_int
     lib.mla_combine_planned.argtypes = [P, sz, i32, i32, P, P, P]
     lib.mla_combine_planned.restype = ctypes.c_int
-    # the split form works on the kernel's 128 heads; fewer go through mla_decode(_planned)
-    assert lib.mla_decode_partial(None, None, None, 1, 64, None, 1, None, 2, 16, 1, 0.1, None,
+    # the split form takes the few-head kernel's 1 to 32 heads or the pair
+    # kernel's 128; 33 to 127 go through mla_decode(_planned), padded to 128
+    assert lib.mla_decode_partial(None, None, None, 1, 64, None, 1, None, 2, 64, 1, 0.1, None,
                                   None, None, 0, None, None) == 2
-    assert lib.mla_combine_planned(None, 0, 2, 16, None, None, None) == 2
+    assert lib.mla_combine_planned(None, 0, 2, 64, None, None, None) == 2
+    # 16 heads pass the head check and stop at the null pointers ...
+    assert lib.mla_decode_partial(None, None, None, 1, 64, None, 1, None, 2, 16, 1, 0.1, None,
+                                  None, None, 0, None, None) == 1
+    assert lib.mla_combine_planned(None, 0, 2, 16, None, None, None) == 1
+    # ... but the fused append needs all 128
+    kv_new = ctypes.c_void_p(256)
+    assert lib.mla_decode_partial(None, None, kv_new, 1, 64, None, 1, None, 2, 16, 1, 0.1, None,
+                                  None, None, 0, None, None) == 2
     lib.mla_decode_workspace_size.argtypes = [i32, i32]
     lib.mla_decode_workspace_size.restype = sz
     assert lib.mla_decode_workspace_size(4, 129) == 0
