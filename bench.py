@@ -588,15 +588,30 @@ def measure_tp_rank(device, stream, hbm_peak, dp_ms_step, layers, distinct=4, re
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         step()
-    graph.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(reps):
+    with torch.cuda.stream(stream):  # replays run on the current stream
         graph.replay()
-    e1.record(stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / reps
+    # the decode kernel alone (no plan, no combine), eager, events around each launch
+    kern = []
+    with torch.cuda.stream(stream):
+        for r in range(2 * distinct):
+            d = lay[r % distinct]
+            k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            k0.record(stream)
+            mla.mla_decode_partial(d["q"], d["cache"], bt, seq, mi.SOFTMAX_SCALE, out, lse,
+                                   workspace=ws, dev_status=status, stream=sh)
+            k1.record(stream)
+            kern.append((k0, k1))
+    torch.cuda.synchronize()
+    kern_us = sum(a.elapsed_time(b) for a, b in kern[distinct:]) * 1e3 / distinct
+    layer_bytes = B * L_tok * mi.ROW * 2 + B * heads * mi.ROW * 2  # cache rows + q
     cache_bytes = B * L_tok * mi.ROW * 2 * layers
     return {"what": "one TP=8 rank: the node batch of 159 x 4096 sequences, 16 heads "
                     "(the few-head kernel), decoded over every layer's full cache",
@@ -604,7 +619,9 @@ def measure_tp_rank(device, stream, hbm_peak, dp_ms_step, layers, distinct=4, re
             "cache_gb_per_step": round(cache_bytes / 1e9, 3),
             "cache_gbs": round(cache_bytes / (ms * 1e-3) / 1e9, 1),
             "frac_of_hbm_peak": round(cache_bytes / (ms * 1e-3) / 1e9 / hbm_peak, 4),
-            "vs_dp_rank_step": round(ms / dp_ms_step, 2),
+            "vs_dp_rank_step": round(ms / dp_ms_step, 2) if dp_ms_step else None,
+            "decode_kernel_us": round(kern_us, 2),
+            "decode_kernel_frac_of_hbm_peak": round(layer_bytes / (kern_us * 1e-6) / 1e9 / hbm_peak, 4),
             "caches": f"{distinct} distinct layer caches of {B * L_tok * mi.ROW * 2 / 1e9:.2f} GB, "
                       f"cycled"}
 
@@ -779,10 +796,22 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--layers", type=int, default=0,
                     help="run only the first N layers of the workload (for profiling captures)")
+    ap.add_argument("--tp-only", action="store_true",
+                    help="time only one TP=8 rank's step (16 heads; --layers sets its layers) "
+                         "and print that object")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     rank, world, local_rank = dist_env()
+    if args.tp_only:
+        import torch
+        torch.cuda.set_device(local_rank)
+        device = torch.device("cuda", local_rank)
+        hbm_peak = measured_peaks()[0]
+        res = measure_tp_rank(device, torch.cuda.Stream(), hbm_peak, None, args.layers or 61)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        return
     w = mi.workload(args.config)
     if args.layers and args.layers < w.layers:
         import dataclasses

@@ -23,8 +23,9 @@
 //
 // Layout of the work.  One CTA per SM and one split range of the plan (64-token
 // units, common.cuh) per CTA.  A tile is 64 tokens of all 576 dims, 72 KB in
-// nine 64-dim chunks with the 128-byte swizzle, fetched by one 3-D TMA box
-// when a page holds 64 tokens or more; two ring slots.  Tensor memory holds
+// nine 64-dim chunks with the 128-byte swizzle, fetched by three 3-D TMA boxes
+// (value dims 0-255, 256-511, rope) when a page holds 64 tokens or more; two
+// ring slots.  Tensor memory holds
 // O^T (four blocks of kHP columns, all 128 lanes: lane = value dim) and two S^T
 // buffers of kHP columns (an M = 64 result puts rows 16q .. 16q + 15 in lanes
 // 32q .. 32q + 15).
@@ -53,26 +54,42 @@ namespace tp {
 
 using namespace sm100;
 
-constexpr int kTile = 64;                          // tokens per tile (= plan unit)
-constexpr int kSlots = 2;                          // tile ring slots
-constexpr int kChunks = kRow / 64;                 // 9 chunks of 64 dims per row
-constexpr int kChunkBytes = kTile * 128;           // 8 KB: 64 tokens x 64 dims
-constexpr int kSlotBytes = kChunks * kChunkBytes;  // 72 KB
-constexpr int kQBufs = 2;                          // the next segment's Q loads early
+constexpr int kTile = 64;                   // tokens per tile (= plan unit)
+constexpr int kChunks = kRow / 64;          // 9 chunks of 64 dims per row
+constexpr int kChunkBytes = kTile * 128;    // 8 KB: 64 tokens x 64 dims
+constexpr int kHalfChunks = 4;              // a value half: 256 dims
+constexpr int kHalfBytes = kHalfChunks * kChunkBytes;  // 32 KB
+constexpr int kRopeSlots = 2;
+constexpr int kQBufs = 2;                   // the next segment's Q loads early
 constexpr int kThreads = 256;
 constexpr int kSoftmaxWarp0 = 4;
 constexpr uint64_t kWaitBudgetNs = 100000000ull;  // 100 ms per wait, far above any legal wait
 constexpr uint64_t kDrainBudgetNs = 10000000ull;  // 10 ms to drain in-flight copies on abort
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
 
+// Ring slots of value halves: as many as shared memory holds beside the rope
+// ring, two Q buffers and P^T (5 at 16 heads: 2.5 tiles of values in flight).
+template <int kHP>
+constexpr int half_slots() {
+  return kHP == 16 ? 5 : 4;
+}
+
+// A tile arrives as three boxes with their own barriers: value dims 0-255
+// (half 0, chunks 0-3), 256-511 (half 1, chunks 4-7) and the rope (chunk 8).
+// The halves share one ring and the rope has its own, because they are freed
+// at different times: a half once the O^T MMAs of its two blocks are done,
+// the rope once the tile's S^T MMAs are.  Half h of tile g is the ring's
+// item 2g + h.
 template <int kHP>
 struct __align__(1024) Smem {
-  uint8_t kv[kSlots][kSlotBytes];         // tile: chunk c at + 8 KB c, token r at + 128 r
-  uint8_t q[kQBufs][kChunks][kHP * 128];  // Q of a segment: chunk c = kHP heads x 64 dims
-  uint8_t p[2][kHP * 128];                // P^T of a tile: row h = the tile's 64 tokens (bf16)
-  float red[2][kHP][4];                   // each softmax warp's tile max of every head
-  float redl[kHP][4];                     // each softmax warp's sum of every head
-  uint64_t full[kSlots], empty[kSlots];
+  uint8_t kv[half_slots<kHP>()][kHalfBytes];  // chunk c of a half at + 8 KB c, token r at + 128 r
+  uint8_t rope[kRopeSlots][kChunkBytes];
+  uint8_t q[kQBufs][kChunks][kHP * 128];      // Q of a segment: chunk c = kHP heads x 64 dims
+  uint8_t p[2][kHP * 128];                    // P^T of a tile: row h = the tile's 64 tokens (bf16)
+  float red[2][kHP][4];                       // each softmax warp's tile max of every head
+  float redl[kHP][4];                         // each softmax warp's sum of every head
+  uint64_t kv_full[half_slots<kHP>()], kv_empty[half_slots<kHP>()];
+  uint64_t rope_full[kRopeSlots], rope_empty[kRopeSlots];
   uint64_t q_full[kQBufs], q_free[kQBufs];
   // S^T buffer written / read by all softmax warps; P^T written; O^T MMAs of
   // the tile done; the four warps' maxima (sums) in red (redl)
@@ -92,7 +109,8 @@ constexpr uint32_t tmem_cols() {
 }
 
 struct Maps {
-  CUtensorMap kv9;   // {64, rows, 9 chunks}, box {64, 64, 9}: one tile
+  CUtensorMap kv4;   // {64, rows, 9 chunks}, box {64, 64, 4}: value dims of a tile part
+  CUtensorMap kv1;   // the same view, box {64, 64, 1}: the rope chunk
   CUtensorMap kv2d;  // {576, rows}, box {64, block_size}: one chunk of one page
   CUtensorMap q;     // {64, batch * heads, 9 chunks}, box {64, kHP, 9}
 };
@@ -160,6 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     decode_tp_kernel(const __grid_constant__ Maps maps, const Params prm) {
   constexpr uint32_t kColO = 0, kColS = 4 * kHP, kCols = tmem_cols<kHP>();
   constexpr int kQBytes = kChunks * kHP * 128;
+  constexpr int kHalves = half_slots<kHP>();
   extern __shared__ uint8_t smem_raw[];
   Smem<kHP> &s = *reinterpret_cast<Smem<kHP> *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -170,9 +189,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const SegRec seg_first = v.seg_rec[(int64_t)range * kSegCache];
 
   if (tid == 0) {
-    for (int i = 0; i < kSlots; ++i) {
-      mbar_init(smem_u32(&s.full[i]), 1);
-      mbar_init(smem_u32(&s.empty[i]), 1);
+    for (int i = 0; i < kHalves; ++i) {
+      mbar_init(smem_u32(&s.kv_full[i]), 1);
+      mbar_init(smem_u32(&s.kv_empty[i]), 1);
+    }
+    for (int i = 0; i < kRopeSlots; ++i) {
+      mbar_init(smem_u32(&s.rope_full[i]), 1);
+      mbar_init(smem_u32(&s.rope_empty[i]), 1);
     }
     for (int i = 0; i < kQBufs; ++i) {
       mbar_init(smem_u32(&s.q_full[i]), 1);
@@ -212,10 +235,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       it.init(v, prm.batch, range, seg_n, seg_first);
       int32_t t0, t1, slot_p;
       uint32_t g = 0;
-      uint32_t issued[kSlots] = {0, 0};
+      uint32_t half_issued[kHalves] = {}, rope_issued[kRopeSlots] = {};
       const int box_rows = big_pages ? kTile : BS;
       const int64_t nb = prm.num_blocks;
-      prefetch_tmap(big_pages ? &maps.kv9 : &maps.kv2d);
+      if (big_pages) {
+        prefetch_tmap(&maps.kv4);
+        prefetch_tmap(&maps.kv1);
+      } else {
+        prefetch_tmap(&maps.kv2d);
+      }
       bool ok = true;
       while (ok && it.next(t0, t1, slot_p)) {
         const int32_t *row = prm.block_table + (int64_t)it.b * prm.max_blocks_per_seq;
@@ -238,33 +266,63 @@ __global__ void __launch_bounds__(kThreads, 1)
               y[j] = blk * BS + (tt + j * box_rows) % BS;
             }
           }
-          const int slot = g % kSlots;
-          if (!mbar_wait(smem_u32(&s.empty[slot]), ((g / kSlots) & 1u) ^ 1u, abort_flag,
+          // the two value halves, then the rope, each once its slot is free
+          for (int hf = 0; hf < 2; ++hf) {
+            const uint32_t k = 2 * g + hf;
+            const int sl = k % kHalves;
+            if (!mbar_wait(smem_u32(&s.kv_empty[sl]), ((k / kHalves) & 1u) ^ 1u, abort_flag,
+                           kWaitBudgetNs)) {
+              set_abort(s, prm.dev_status);
+              ok = false;
+              break;
+            }
+            const uint32_t bar = smem_u32(&s.kv_full[sl]);
+            mbar_arrive_expect_tx(bar, (uint32_t)(kHalfChunks * nbx * box_rows * 128));
+            if (big_pages) {
+              tma_load_3d(smem_u32(s.kv[sl]), &maps.kv4, 0, y[0], kHalfChunks * hf, bar);
+            } else {
+#pragma unroll
+              for (int j = 0; j < kTile / 16; ++j) {
+                if (j >= nbx) break;
+                for (int c = 0; c < kHalfChunks; ++c)
+                  tma_load_2d(smem_u32(s.kv[sl]) + c * kChunkBytes + j * box_rows * 128,
+                              &maps.kv2d, 64 * (kHalfChunks * hf + c), y[j], bar);
+              }
+            }
+            ++half_issued[sl];
+          }
+          if (!ok) break;
+          const int rs = g % kRopeSlots;
+          if (!mbar_wait(smem_u32(&s.rope_empty[rs]), ((g / kRopeSlots) & 1u) ^ 1u, abort_flag,
                          kWaitBudgetNs)) {
             set_abort(s, prm.dev_status);
             ok = false;
             break;
           }
-          const uint32_t bar = smem_u32(&s.full[slot]);
-          mbar_arrive_expect_tx(bar, (uint32_t)(kChunks * nbx * box_rows * 128));
+          const uint32_t rbar = smem_u32(&s.rope_full[rs]);
+          mbar_arrive_expect_tx(rbar, (uint32_t)(nbx * box_rows * 128));
           if (big_pages) {
-            tma_load_3d(smem_u32(s.kv[slot]), &maps.kv9, 0, y[0], 0, bar);
+            tma_load_3d(smem_u32(s.rope[rs]), &maps.kv1, 0, y[0], kChunks - 1, rbar);
           } else {
 #pragma unroll
             for (int j = 0; j < kTile / 16; ++j) {
               if (j >= nbx) break;
-              for (int c = 0; c < kChunks; ++c)
-                tma_load_2d(smem_u32(s.kv[slot]) + c * kChunkBytes + j * box_rows * 128,
-                            &maps.kv2d, 64 * c, y[j], bar);
+              tma_load_2d(smem_u32(s.rope[rs]) + j * box_rows * 128, &maps.kv2d,
+                          64 * (kChunks - 1), y[j], rbar);
             }
           }
-          ++issued[slot];
+          ++rope_issued[rs];
         }
       }
       if (s.abort) {  // let the loads in flight land before exit
-        for (int i = 0; i < kSlots; ++i)
-          if (issued[i] > 0)
-            (void)mbar_wait(smem_u32(&s.full[i]), (issued[i] - 1) & 1u, nullptr, kDrainBudgetNs);
+        for (int i = 0; i < kHalves; ++i)
+          if (half_issued[i] > 0)
+            (void)mbar_wait(smem_u32(&s.kv_full[i]), (half_issued[i] - 1) & 1u, nullptr,
+                            kDrainBudgetNs);
+        for (int i = 0; i < kRopeSlots; ++i)
+          if (rope_issued[i] > 0)
+            (void)mbar_wait(smem_u32(&s.rope_full[i]), (rope_issued[i] - 1) & 1u, nullptr,
+                            kDrainBudgetNs);
       }
     }
   } else if (warp == 1) {
@@ -279,6 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // k-steps add their byte offset >> 4 to the start-address field (no
       // carry: every shared-memory address here is below 2^18)
       const uint64_t d_kv = smem_desc(smem_u32(s.kv[0]), 16, 1024, kSwizzle128B);
+      const uint64_t d_rope = smem_desc(smem_u32(s.rope[0]), 16, 1024, kSwizzle128B);
       const uint64_t d_q = smem_desc(smem_u32(s.q[0][0]), 16, 1024, kSwizzle128B);
       bool ok = true;
       while (ok && it.next(t0, t1, slot_p)) {
@@ -289,27 +348,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++seg;
         for (int32_t tt = t0; tt < t1; tt += kTile, ++g) {
-          const int slot = g % kSlots;
           // the S^T buffer was last read by the softmax of tile g - 2
-          if ((g >= 2 && !mbar_wait(smem_u32(&s.s_free[g & 1u]), ((g >> 1) - 1) & 1u, abort_flag,
-                                    kWaitBudgetNs)) ||
-              !mbar_wait(smem_u32(&s.full[slot]), (g / kSlots) & 1u, abort_flag, kWaitBudgetNs)) {
+          if (g >= 2 && !mbar_wait(smem_u32(&s.s_free[g & 1u]), ((g >> 1) - 1) & 1u, abort_flag,
+                                   kWaitBudgetNs)) {
+            set_abort(s, prm.dev_status);
+            ok = false;
+            break;
+          }
+          const uint32_t d_s = tmem + kColS + kHP * (g & 1u);
+          const uint64_t b0 = d_q + (uint64_t)((qb * kQBytes) >> 4);
+          for (int hf = 0; hf < 2 && ok; ++hf) {
+            const uint32_t k = 2 * g + hf;
+            const int sl = k % kHalves;
+            if (!mbar_wait(smem_u32(&s.kv_full[sl]), (k / kHalves) & 1u, abort_flag,
+                           kWaitBudgetNs)) {
+              set_abort(s, prm.dev_status);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t a0 = d_kv + (uint64_t)((sl * kHalfBytes) >> 4);
+#pragma unroll
+            for (int c = 0; c < kHalfChunks; ++c) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_ss(d_s, a0 + (uint64_t)((c * kChunkBytes + kk * 32) >> 4),
+                       b0 + (uint64_t)((((kHalfChunks * hf + c) * kHP * 128) + kk * 32) >> 4), id,
+                       (hf | c | kk) ? 1u : 0u);
+            }
+          }
+          if (!ok) break;
+          const int rs = g % kRopeSlots;
+          if (!mbar_wait(smem_u32(&s.rope_full[rs]), (g / kRopeSlots) & 1u, abort_flag,
+                         kWaitBudgetNs)) {
             set_abort(s, prm.dev_status);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t d_s = tmem + kColS + kHP * (g & 1u);
-          const uint64_t a0 = d_kv + (uint64_t)((slot * kSlotBytes) >> 4);
-          const uint64_t b0 = d_q + (uint64_t)((qb * kQBytes) >> 4);
+          const uint64_t r0 = d_rope + (uint64_t)((rs * kChunkBytes) >> 4);
 #pragma unroll
-          for (int c = 0; c < kChunks; ++c) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ss(d_s, a0 + (uint64_t)((c * kChunkBytes + kk * 32) >> 4),
-                     b0 + (uint64_t)((c * kHP * 128 + kk * 32) >> 4), id, (c | kk) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(d_s, r0 + (uint64_t)((kk * 32) >> 4),
+                   b0 + (uint64_t)((((kChunks - 1) * kHP * 128) + kk * 32) >> 4), id, 1u);
           mma_commit(smem_u32(&s.s_full[g & 1u]));
+          mma_commit(smem_u32(&s.rope_empty[rs]));  // the rope is read by S^T only
         }
         if (!ok) break;
         mma_commit(smem_u32(&s.q_free[qb]));  // this segment's Q is no longer read
@@ -332,7 +415,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       while (ok && it.next(t0, t1, slot_p)) {
         for (int32_t tt = t0; tt < t1; tt += kTile, ++g) {
-          const int slot = g % kSlots;
           if (!mbar_wait(smem_u32(&s.p_full[g & 1u]), (g >> 1) & 1u, abort_flag, kWaitBudgetNs)) {
             set_abort(s, prm.dev_status);
             ok = false;
@@ -340,16 +422,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const int ksteps = (min(kTile, t1 - tt) + 15) >> 4;
-          const uint64_t a0 = d_v + (uint64_t)((slot * kSlotBytes) >> 4);
           const uint64_t b0 = d_p + (uint64_t)(((g & 1u) * kHP * 128) >> 4);
+          // block i = 2 hf + ib: value dims 128 i .. 128 i + 127, chunks 2 ib and
+          // 2 ib + 1 of half hf; the half's slot is free once its blocks are done
+          for (int hf = 0; hf < 2; ++hf) {
+            const int sl = (2 * g + hf) % kHalves;
+            const uint64_t a0 = d_v + (uint64_t)((sl * kHalfBytes) >> 4);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            for (int kt = 0; kt < ksteps; ++kt)
-              mma_ss(tmem + kColO + i * kHP,
-                     a0 + (uint64_t)((2 * i * kChunkBytes + kt * 2048) >> 4),
-                     b0 + (uint64_t)((kt * 32) >> 4), id, (tt > t0 || kt > 0) ? 1u : 0u);
+            for (int ib = 0; ib < 2; ++ib) {
+              for (int kt = 0; kt < ksteps; ++kt)
+                mma_ss(tmem + kColO + (2 * hf + ib) * kHP,
+                       a0 + (uint64_t)((2 * ib * kChunkBytes + kt * 2048) >> 4),
+                       b0 + (uint64_t)((kt * 32) >> 4), id, (tt > t0 || kt > 0) ? 1u : 0u);
+            }
+            mma_commit(smem_u32(&s.kv_empty[sl]));
           }
-          mma_commit(smem_u32(&s.empty[slot]));
           mma_commit(smem_u32(&s.pv_done[g & 1u]));
         }
       }
@@ -502,11 +589,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           // sequence end hold whatever the page held (maybe NaN; 0 * NaN = NaN),
           // so zero them in the eight value chunks (whole 128-byte rows).
           if (n & 15) {
-            uint8_t *base = s.kv[g % kSlots];
             const int rows = ((n + 15) & ~15) - n;
             for (int k = st; k < rows * 64; k += 128) {
               const int r = n + (k >> 6), ch = (k >> 3) & 7, u = k & 7;
-              *reinterpret_cast<uint4 *>(base + ch * kChunkBytes + r * 128 + u * 16) =
+              uint8_t *half = s.kv[(2 * g + (ch >> 2)) % kHalves];
+              *reinterpret_cast<uint4 *>(half + (ch & 3) * kChunkBytes + r * 128 + u * 16) =
                   make_uint4(0, 0, 0, 0);
             }
           }
@@ -617,7 +704,7 @@ struct TpKvEntry {
   const void *base;
   int64_t rows;
   int32_t block_size;
-  CUtensorMap kv9, kv2d;
+  CUtensorMap kv4, kv1, kv2d;
 };
 struct TpQEntry {
   bool valid;
@@ -639,7 +726,8 @@ bool tp_maps(int dev, const void *cache, int64_t rows, int32_t block_size, const
         e.block_size == block_size)) {
     const uint32_t box_rows = block_size < tp::kTile ? (uint32_t)block_size : (uint32_t)tp::kTile;
     e.valid = false;
-    if (!tmap::encode_3d(&e.kv9, cache, rows, box_rows, tp::kChunks) ||
+    if (!tmap::encode_3d(&e.kv4, cache, rows, box_rows, 4) ||
+        !tmap::encode_3d(&e.kv1, cache, rows, box_rows, 1) ||
         !tmap::encode_2d(&e.kv2d, cache, rows, box_rows))
       return false;
     e.valid = true;
@@ -658,7 +746,8 @@ bool tp_maps(int dev, const void *cache, int64_t rows, int32_t block_size, const
     f.rows = q_rows;
     f.box_rows = hp;
   }
-  m->kv9 = e.kv9;
+  m->kv4 = e.kv4;
+  m->kv1 = e.kv1;
   m->kv2d = e.kv2d;
   m->q = f.q;
   return true;
