@@ -150,12 +150,17 @@ mla_status_t mla_decode_plan(const int32_t *seq_lens, const int32_t *block_table
  *                 do not matter (the plan rewrites everything the decode
  *                 reads).  Calls sharing one workspace must not overlap on
  *                 the GPU.
- * Requirements: 1 <= num_heads <= 128 (mla_decode and mla_decode_planned;
- * below 128 — a tensor-parallel rank's share of the heads, e.g. 16 at TP = 8
- * [dp-attention-expert-parallel-mla-kv-replication (inferenceinterviews.com),
- * "A strong answer"] — q is padded to 128 heads inside the workspace, which
- * mla_decode_workspace_size(batch, num_heads) sizes for it; the other decode
- * entry points need 128); block_size in {16, 32, 64, 128, 256};
+ * Heads: 1 <= num_heads <= 128.  128 heads run on the tensor-core kernel
+ * whose CTA pairs split the output dims; 1 to 32 heads — a tensor-parallel
+ * rank's share, e.g. 16 at TP = 8 [dp-attention-expert-parallel-mla-kv-
+ * replication (inferenceinterviews.com), "A strong answer"] — run on a
+ * kernel of their own, which computes the transposed products (tokens and
+ * value dims in the MMA's M, heads in N) with one CTA per SM; 33 to 127 are
+ * padded to 128 inside the workspace (mla_decode and mla_decode_planned
+ * only).  mla_decode_workspace_size(batch, num_heads) sizes the workspace
+ * for the path num_heads takes, and mla_decode_plan must be given the same
+ * num_heads as the decode that uses its plan.
+ * Requirements: block_size in {16, 32, 64, 128, 256};
  * max_seq_len <= max_blocks_per_seq * block_size <= 2^30; batch *
  * ceil(max_blocks_per_seq * block_size / 64) < 2^31 (the plan counts 64-token
  * units in int32); batch >= 0 (0 = no-op).  Else MLA_ERR_INVALID_ARGUMENT.
@@ -192,8 +197,9 @@ mla_status_t mla_decode_planned(const void *q, const void *cache, int64_t num_bl
  * each request's new row as mla_decode_append_planned does (the cache is
  * written then; with kv_new NULL it is only read).  mla_combine_planned then
  * merges the partials into out / lse (requests that were not split are left
- * as they are).  Same arguments and requirements as mla_decode_planned; the
- * workspace must not be touched between the two calls.
+ * as they are).  Same arguments and requirements as mla_decode_planned, with
+ * num_heads 128 or 1 to 32 (else MLA_ERR_UNSUPPORTED); kv_new needs 128
+ * heads.  The workspace must not be touched between the two calls.
  */
 mla_status_t mla_decode_partial(const void *q, void *cache, const void *kv_new,
                                 int64_t num_blocks, int32_t block_size,
@@ -326,9 +332,8 @@ mla_status_t mla_decode_fp8_planned(const void *q, void *cache8, const void *kv_
  * 16 MiB until the process exits.  It calls no cudaMalloc, cudaFree or other
  * allocating routine.
  *
- * Limits: num_heads must be 128 (the tensor-parallel head counts that
- * mla_decode accepts pad q into its workspace, which this entry point does
- * not have; other values return MLA_ERR_UNSUPPORTED); batch <=
+ * Limits: num_heads must be 128 (other values return MLA_ERR_UNSUPPORTED;
+ * mla_decode takes 1 to 128); batch <=
  * MLA_NOALLOC_MAX_BATCH (8192), else MLA_ERR_INVALID_ARGUMENT with an
  * explanatory detail.  Because the scratch holds fewer split partials than a
  * full workspace, long contexts are spread over fewer SMs than with
