@@ -12,6 +12,10 @@ namespace mla {
 
 constexpr int kPlanThreads = 1024;
 constexpr int kMaxPlanRanges = 1024;  // boundaries are settled in shared memory
+// Batches up to this size keep their prefixes and lengths in shared memory
+// too, so the planner's binary searches and walks make no global round trips
+// (larger batches read them back from the workspace).
+constexpr int kPlanSmemBatch = 2048;
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__restrict__ seq_lens,
                                                             const int32_t *__restrict__ block_table,
@@ -30,6 +34,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
   __shared__ int64_t warp_sums[kPlanThreads / 32];
   __shared__ int64_t carry;
   __shared__ int32_t bound[kMaxPlanRanges + 1];
+  __shared__ int32_t s_rfirst[kMaxPlanRanges];
+  __shared__ int32_t s_prefix[kPlanSmemBatch + 1], s_seq[kPlanSmemBatch];
+  __shared__ int64_t s_cost[kPlanSmemBatch + 1];
+  const bool small = batch <= kPlanSmemBatch;
+  // where the phases below read the prefixes and clamped lengths back from
+  const int32_t *pre = small ? s_prefix : prefix;
+  const int64_t *cpre = small ? s_cost : cost_prefix;
+  const int32_t *sq = small ? s_seq : seq_out;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int64_t max_len = (int64_t)max_blocks_per_seq * block_size;
   if (tid == 0) carry = 0;
@@ -47,6 +59,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
         L = L < 0 ? 0 : (int32_t)max_len;
       }
       seq_out[b] = L;
+      if (small) s_seq[b] = L;
       const int32_t units = (L + unit_tokens - 1) / unit_tokens;
       item = units > 0 ? (int64_t(1) << 32) | units : 0;
       v.counters[2 * b] = 0;
@@ -73,8 +86,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
     const int64_t incl = x + (wid > 0 ? warp_sums[wid - 1] : 0) + carry;
     if (b < batch) {
       const int64_t excl = incl - item;
-      prefix[b] = (int32_t)(excl & 0xffffffff);
-      cost_prefix[b] = kUnitCost * (excl & 0xffffffff) + kSegmentCost * (excl >> 32);
+      const int32_t pb = (int32_t)(excl & 0xffffffff);
+      const int64_t cb = kUnitCost * (excl & 0xffffffff) + kSegmentCost * (excl >> 32);
+      prefix[b] = pb;
+      cost_prefix[b] = cb;
+      if (small) {
+        s_prefix[b] = pb;
+        s_cost[b] = cb;
+      }
     }
     __syncthreads();
     if (tid == kPlanThreads - 1) carry = incl;
@@ -85,7 +104,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
   if (tid == 0) {
     prefix[batch] = U;
     cost_prefix[batch] = C;
+    if (small) {
+      s_prefix[batch] = U;
+      s_cost[batch] = C;
+    }
   }
+  __syncthreads();  // the shared copies are complete
   const int32_t P = U < max_ranges ? U : max_ranges;
   // Range boundaries.  First the unit at cost p*C/P, held as R_p - p ...
   for (int p = tid; p <= P; p += kPlanThreads) {
@@ -97,12 +121,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
       int lo = 0, hi = batch - 1;  // the request whose cost span holds c
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (cost_prefix[mid] <= c) lo = mid; else hi = mid - 1;
+        if (cpre[mid] <= c) lo = mid; else hi = mid - 1;
       }
-      const int64_t x = c - cost_prefix[lo];
+      const int64_t x = c - cpre[lo];
       const int64_t k = x < kSegmentCost ? 0 : (x - kSegmentCost + kUnitCost / 2) / kUnitCost;
-      const int32_t n = prefix[lo + 1] - prefix[lo];
-      r = prefix[lo] + (int32_t)(k < n ? k : n);
+      const int32_t n = pre[lo + 1] - pre[lo];
+      r = pre[lo] + (int32_t)(k < n ? k : n);
     }
     bound[p] = r - p;
   }
@@ -150,9 +174,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
     int lo = 0, hi = batch - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (prefix[mid] <= r) lo = mid; else hi = mid - 1;
+      if (pre[mid] <= r) lo = mid; else hi = mid - 1;
     }
     range_first[p] = lo;
+    s_rfirst[p] = lo;
   }
   __syncthreads();  // range_first, prefix and the clamped lengths are visible to the block
   // every request's split, for the combine (see ReqSplit)
@@ -166,7 +191,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
   };
   ReqSplit *req_split = const_cast<ReqSplit *>(v.req_split);
   for (int b = tid; b < batch; b += kPlanThreads) {
-    const int32_t Ub = prefix[b], n = prefix[b + 1] - Ub;
+    const int32_t Ub = pre[b], n = pre[b + 1] - Ub;
     ReqSplit r;
     r.p0 = n > 0 ? range_of(Ub) : 0;
     r.p1 = n > 0 ? range_of(Ub + n - 1) : 0;
@@ -181,15 +206,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
     int32_t n = 0;
     if (p < P) {
       const int32_t r0 = bound[p], r1 = bound[p + 1];
-      for (int b = range_first[p]; b < batch && prefix[b] < r1; ++b) {
-        const int32_t Ub = prefix[b], Ue = prefix[b + 1];
+      for (int b = s_rfirst[p]; b < batch && pre[b] < r1; ++b) {
+        const int32_t Ub = pre[b], Ue = pre[b + 1];
         const int32_t u0 = max(r0, Ub), u1 = min(r1, Ue);
         if (u0 >= u1) continue;
         if (n < kSegCache) {
           SegRec r;
           r.b = b;
           r.t0 = (u0 - Ub) * unit_tokens;
-          r.t1 = min((u1 - Ub) * unit_tokens, seq_out[b]);
+          r.t1 = min((u1 - Ub) * unit_tokens, sq[b]);
           r.slot = segment_slot(p, r0, r1, Ub, Ue);
           r.row0 = -1;
           if (block_table && block_size >= unit_tokens && r.t0 < r.t1) {
@@ -303,12 +328,13 @@ __device__ __forceinline__ void combine_row(const float *__restrict__ o_part,
 // output dims.  With one split lane (kLanes = 1) its thread h is head h and
 // merges all the request's splits, four at a time with their loads all in
 // flight before any is used (a warp's 16-byte loads are 512 contiguous bytes
-// of 32 heads), in fp32.  With four split lanes (kLanes = 4; for small batches, whose
-// requests are spread over many ranges) a block takes 32 heads, and warp s
-// merges splits s, s + 4, s + 8, ... of them; the four running results of a
-// head (max, weight sum, 16 weighted dims) are then merged through shared
-// memory, one warp per four dims.  The bf16 results leave as 32-byte row
-// pieces.  grid = (batch, 512 / 16, kLanes), 128 threads.
+// of 32 heads), in fp32.  With kLanes = 4 or 16 split lanes (small batches,
+// whose requests are spread over many ranges) a block takes 128 / kLanes
+// heads, and lane s (threads s * 128 / kLanes ...) merges splits s, s + kLanes,
+// s + 2 kLanes, ... of them; the kLanes running results of a head (max, weight
+// sum, 16 weighted dims) are then merged through shared memory, each thread
+// finishing 16 / kLanes dims of one head.  The bf16 results leave as 32-byte
+// row pieces.  grid = (batch, 512 / 16, kLanes), 128 threads.
 constexpr int kCombDims = 16;
 constexpr int kCombGroup = 4;  // splits per lane whose loads are in flight together
 
@@ -320,8 +346,8 @@ __global__ void __launch_bounds__(kHeads) plan_combine_kernel(void *ws, int32_t 
   constexpr int kBlockHeads = kHeads / kLanes;
   PlanView v = plan_view(ws, batch, kHeads, max_ranges);
   const int b = blockIdx.x, d0 = blockIdx.y * kCombDims;
-  const int sl = kLanes == 1 ? 0 : (int)(threadIdx.x >> 5);  // split lane
-  const int hb = kLanes == 1 ? (int)threadIdx.x : (int)(threadIdx.x & 31);  // head in the block
+  const int sl = (int)threadIdx.x / kBlockHeads;  // split lane
+  const int hb = (int)threadIdx.x % kBlockHeads;  // head in the block
   const int h = blockIdx.z * kBlockHeads + hb;
   const ReqSplit rs = v.req_split[b];
   if (rs.p0 == rs.p1) return;  // not split (or empty): the decode wrote it
@@ -390,34 +416,41 @@ __global__ void __launch_bounds__(kHeads) plan_combine_kernel(void *ws, int32_t 
     }
     if (lse && blockIdx.y == 0) lse[(int64_t)b * kHeads + h] = z > 0.f ? m + logf(z) : -INFINITY;
   } else {
+    constexpr int kDimsPerThread = kCombDims / kLanes;
     __shared__ float s_m[kLanes][kBlockHeads], s_z[kLanes][kBlockHeads];
-    __shared__ float4 s_acc[kLanes][kCombDims / 4][kBlockHeads];
+    __shared__ float s_acc[kLanes][kCombDims][kBlockHeads];
     s_m[sl][hb] = m;
     s_z[sl][hb] = z;
 #pragma unroll
-    for (int j = 0; j < kCombDims / 4; ++j) s_acc[sl][j][hb] = acc[j];
+    for (int j = 0; j < kCombDims / 4; ++j) {
+      s_acc[sl][4 * j][hb] = acc[j].x;
+      s_acc[sl][4 * j + 1][hb] = acc[j].y;
+      s_acc[sl][4 * j + 2][hb] = acc[j].z;
+      s_acc[sl][4 * j + 3][hb] = acc[j].w;
+    }
     __syncthreads();
-    // warp sl finishes dims [4 sl, 4 sl + 4) of the block's heads
+    // thread (sl, hb) finishes dims [sl kDimsPerThread, (sl + 1) kDimsPerThread) of head hb
     float M = -INFINITY;
 #pragma unroll
     for (int i = 0; i < kLanes; ++i) M = fmaxf(M, s_m[i][hb]);
     float Z = 0.f;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    float o[kDimsPerThread];
+#pragma unroll
+    for (int j = 0; j < kDimsPerThread; ++j) o[j] = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
       for (int i = 0; i < kLanes; ++i) {
         const float mi = s_m[i][hb];
         const float a = mi == -INFINITY ? 0.f : __expf(mi - M);
-        const float4 xx = s_acc[i][sl][hb];
         Z += a * s_z[i][hb];
-        o.x += a * xx.x; o.y += a * xx.y; o.z += a * xx.z; o.w += a * xx.w;
+#pragma unroll
+        for (int j = 0; j < kDimsPerThread; ++j) o[j] += a * s_acc[i][sl * kDimsPerThread + j][hb];
       }
     }
     const float inv = Z > 0.f ? 1.f / Z : 0.f;
-    *reinterpret_cast<__nv_bfloat162 *>(&tile[hb][4 * sl]) =
-        __floats2bfloat162_rn(o.x * inv, o.y * inv);
-    *reinterpret_cast<__nv_bfloat162 *>(&tile[hb][4 * sl + 2]) =
-        __floats2bfloat162_rn(o.z * inv, o.w * inv);
+#pragma unroll
+    for (int j = 0; j < kDimsPerThread; ++j)
+      tile[hb][sl * kDimsPerThread + j] = __float2bfloat16_rn(o[j] * inv);
     if (lse && blockIdx.y == 0 && sl == 0)
       lse[(int64_t)b * kHeads + h] = Z > 0.f ? M + logf(Z) : -INFINITY;
   }
@@ -436,10 +469,15 @@ __global__ void __launch_bounds__(kHeads) plan_combine_kernel(void *ws, int32_t 
 cudaError_t launch_plan_combine(void *ws, int32_t batch, int32_t heads, int32_t max_ranges,
                                 void *out, float *lse, cudaStream_t stream) {
   if (heads != kHeads) return cudaErrorInvalidValue;
-  // Four split lanes when requests average eight or more ranges (a small
-  // batch, where one long request is spread over most of the SM pairs); one
-  // otherwise, so that an ordinary batch keeps one block per 16 dims.
+  // Split lanes when requests average four or more ranges (a small batch,
+  // where one long request may be spread over most of the SM pairs): 16 from
+  // eight ranges a request on average, 4 from four; one otherwise, so that an
+  // ordinary batch keeps one block per 16 dims.
   if ((int64_t)batch * 8 <= max_ranges) {
+    dim3 grid(batch, kVDim / kCombDims, 16);
+    plan_combine_kernel<16><<<grid, kHeads, 0, stream>>>(ws, batch, max_ranges,
+                                                         (__nv_bfloat16 *)out, lse);
+  } else if ((int64_t)batch * 4 <= max_ranges) {
     dim3 grid(batch, kVDim / kCombDims, 4);
     plan_combine_kernel<4><<<grid, kHeads, 0, stream>>>(ws, batch, max_ranges,
                                                         (__nv_bfloat16 *)out, lse);
