@@ -23,12 +23,13 @@
 //
 // Layout of the work.  One CTA per SM and one split range of the plan (64-token
 // units, common.cuh) per CTA.  A tile is 64 tokens of all 576 dims, 72 KB in
-// nine 64-dim chunks with the 128-byte swizzle, fetched by three 3-D TMA boxes
-// (value dims 0-255, 256-511, rope) when a page holds 64 tokens or more; two
-// ring slots.  Tensor memory holds
-// O^T (four blocks of kHP columns, all 128 lanes: lane = value dim) and two S^T
-// buffers of kHP columns (an M = 64 result puts rows 16q .. 16q + 15 in lanes
-// 32q .. 32q + 15).
+// nine 64-dim chunks with the 128-byte swizzle, fetched (when a page holds 64
+// tokens or more) by three 3-D TMA boxes: value dims 0-255 and 256-511 into a
+// ring of 32 KB halves, each freed once its two O^T blocks are done, and the
+// rope chunk into a ring of its own, freed once the scores are.  Tensor memory
+// holds O^T (four blocks of kHP columns, all 128 lanes: lane = value dim) and
+// two S^T buffers of kHP columns (an M = 64 result puts rows 16q .. 16q + 15
+// in lanes 32q .. 32q + 15).
 //
 // Softmax.  A tile's tokens lie across threads (lanes 0-15 of the four
 // softmax warps), so a head's tile max is a reduction across threads: each
