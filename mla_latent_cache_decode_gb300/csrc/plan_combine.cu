@@ -1,7 +1,8 @@
 // Split-KV planner and log-sum-exp combine kernels.
 //
 // The planner turns the (device-resident) sequence lengths into the plan
-// described in common.cuh; the combine kernels merge the fp32 partials of
+// described in common.cuh; the combine kernels merge, in fp32, the partials
+// (bf16 outputs with fp32 log-sum-exps; fp32 for the public mla_combine) of
 // requests that were spread over several workers.  Merging partial softmax
 // results by their log-sum-exp is standard flash-decoding, used here so that
 // one long request does not stall the batch [dp-attention-expert-parallel-mla-
