@@ -106,7 +106,11 @@ mla_status_t mla_cache_append(const void *kv_new, const int64_t *slot_mapping,
  * current device for `batch` requests of `num_heads` heads.  The workspace
  * holds the split plan (units of the token partition, per request) and the
  * partial results of requests that are split across CTAs (each range's
- * normalised output in bf16 with its fp32 log-sum-exp).
+ * normalised output in bf16 with its fp32 log-sum-exp).  It depends on
+ * neither the context lengths nor the page size: the plan has at most one
+ * range per SM pair of the current device (one per SM for 1 to 32 heads)
+ * and each range leaves at most two partials, whatever the lengths.  Returns
+ * 0 for batch < 0, num_heads outside [1, 128] or no current device.
  */
 size_t mla_decode_workspace_size(int32_t batch, int32_t num_heads);
 
