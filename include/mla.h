@@ -57,7 +57,7 @@
 extern "C" {
 #endif
 
-#define MLA_ABI_VERSION 3
+#define MLA_ABI_VERSION 4
 #define MLA_ROW_DIM 576       /* 512 kv_c + 64 k_rope per cached token */
 #define MLA_KV_LORA_RANK 512  /* value / output width */
 #define MLA_ROPE_DIM 64
@@ -70,7 +70,10 @@ typedef enum mla_status {
   MLA_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < mla_decode_workspace_size() */
   MLA_ERR_CUDA = 4,                /* a CUDA runtime call or launch failed */
   MLA_ERR_DEVICE_RANGE = 5,        /* device-seen: bad block id, slot or length */
-  MLA_ERR_DEVICE_TIMEOUT = 6       /* device-seen: a bounded wait expired */
+  MLA_ERR_DEVICE_TIMEOUT = 6,      /* device-seen: a bounded wait expired */
+  MLA_ERR_DEVICE_PLAN = 7          /* device-seen: the workspace holds no plan for these
+                                      arguments (batch, heads, page size, table width);
+                                      nothing was decoded */
 } mla_status_t;
 
 /* Name of a status code ("MLA_OK", ...); never NULL. */
@@ -180,8 +183,15 @@ mla_status_t mla_decode(const void *q, const void *cache, int64_t num_blocks, in
 
 /*
  * mla_decode_planned — mla_decode using the plan already in `workspace`
- * (from mla_decode_plan with the same seq_lens, batch, block_size,
- * max_blocks_per_seq and, if it was given one, block table).  Same arguments and results as mla_decode.
+ * (from mla_decode_plan with the same seq_lens, batch, num_heads, block_size,
+ * max_blocks_per_seq and, if it was given one, block table).  Same arguments
+ * and results as mla_decode.  The planner stamps every segment record with
+ * the arguments it was made for (batch, split ranges, page size, table
+ * width) and the decode checks each record against its own, and against the
+ * bounds of the request, table and workspace, before using it: a plan made
+ * for other arguments is reported as MLA_ERR_DEVICE_PLAN in *dev_status and
+ * out / lse are then unspecified; nothing is read or written out of place,
+ * whatever the workspace holds.
  */
 mla_status_t mla_decode_planned(const void *q, const void *cache, int64_t num_blocks,
                                 int32_t block_size, const int32_t *block_table,

@@ -25,7 +25,7 @@ NUM_HEADS = 128
 
 STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARGUMENT", 2: "MLA_ERR_UNSUPPORTED",
           3: "MLA_ERR_WORKSPACE_TOO_SMALL", 4: "MLA_ERR_CUDA", 5: "MLA_ERR_DEVICE_RANGE",
-          6: "MLA_ERR_DEVICE_TIMEOUT"}
+          6: "MLA_ERR_DEVICE_TIMEOUT", 7: "MLA_ERR_DEVICE_PLAN"}
 EXPORTED = ("mla_status_string", "mla_last_error_detail", "mla_abi_version", "mla_cache_append",
             "mla_decode_workspace_size", "mla_decode_plan", "mla_decode", "mla_decode_planned",
             "mla_combine", "mla_decode_noalloc", "mla_decode_partial", "mla_combine_planned",

@@ -161,6 +161,7 @@ const char *mla_status_string(int status) {
     case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
     case MLA_ERR_DEVICE_RANGE: return "MLA_ERR_DEVICE_RANGE";
     case MLA_ERR_DEVICE_TIMEOUT: return "MLA_ERR_DEVICE_TIMEOUT";
+    case MLA_ERR_DEVICE_PLAN: return "MLA_ERR_DEVICE_PLAN";
     default: return "MLA_ERR_UNKNOWN";
   }
 }

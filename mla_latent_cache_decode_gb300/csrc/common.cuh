@@ -69,8 +69,27 @@ __host__ __device__ inline int32_t segment_slot(int32_t p, int32_t r0, int32_t r
 constexpr int kSegCache = 4;
 struct __align__(16) SegRec {
   int32_t b, t0, t1, slot;
-  int32_t row0, pad0, pad1, pad2;
+  int32_t row0;
+  int32_t stamp;  // plan_stamp of the arguments the plan was made for
+  int32_t pad1, pad2;
 };
+
+// A 32-bit mix of the arguments a plan is made for.  The planner writes it
+// into every segment record and a decode compares it with its own arguments
+// on each record it reads (already in registers: no extra load), so a plan
+// made for another batch, head count, page size or table width is refused.
+__host__ __device__ inline int32_t plan_stamp(int32_t batch, int32_t max_ranges,
+                                              int32_t unit_tokens, int32_t block_size,
+                                              int32_t max_blocks_per_seq) {
+  uint32_t h = 0x6d2b79f5u;
+  const uint32_t parts[5] = {(uint32_t)batch, (uint32_t)max_ranges, (uint32_t)unit_tokens,
+                             (uint32_t)block_size, (uint32_t)max_blocks_per_seq};
+  for (int i = 0; i < 5; ++i) {
+    h ^= parts[i] + 0x9e3779b9u + (h << 6) + (h >> 2);
+    h *= 0x85ebca6bu;
+  }
+  return (int32_t)(h ^ (h >> 15));
+}
 
 // Split of request b, written by the planner for the combine: its partials
 // are in ranges p0..p1 (p0 == p1: not split), stored in slots
@@ -204,7 +223,9 @@ struct SegIter {
     }
     row0 = -1;
     const int32_t r0 = v.range_start[p], r1 = v.range_start[p + 1];
-    for (++b; b < batch; ++b) {
+    // from the request after the last record's (which a plan made for other
+    // arguments may have left anywhere: the walk stays within [0, batch))
+    for (b = (b >= -1 && b < batch) ? b + 1 : batch; b < batch; ++b) {
       const int32_t Ub = v.unit_prefix[b];
       if (Ub >= r1) return false;
       const int32_t Ue = v.unit_prefix[b + 1];
@@ -219,6 +240,20 @@ struct SegIter {
     return false;
   }
 };
+
+// Whether a range's first record (loaded by every thread at kernel entry)
+// belongs to a plan made for these arguments: it carries their stamp and
+// keeps within the request, the block table and the partial slots.  A plan
+// that passes is the one these arguments make, so its other records and
+// arrays are valid too.  Checked once per CTA, before any role reads the
+// plan further (a check inside the segment walk, inlined in every role,
+// measured slower).  A range with no segments reads nothing.
+__device__ __forceinline__ bool plan_record_ok(int32_t seg_n, const SegRec &r, int32_t stamp,
+                                               int32_t batch, int32_t max_len,
+                                               int32_t num_slots) {
+  return seg_n <= 0 || (r.stamp == stamp && r.b >= 0 && r.b < batch && r.t0 >= 0 &&
+                        r.t0 < r.t1 && r.t1 <= max_len && r.slot >= -1 && r.slot < num_slots);
+}
 
 
 }  // namespace mla

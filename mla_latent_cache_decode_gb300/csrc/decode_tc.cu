@@ -282,6 +282,18 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
   const uint32_t tmem = s.tmem_base;
 
   const bool active = seg_n > 0;  // ranges past the plan's count have none
+  // Whether the plan was made for these arguments (see plan_record_ok).  Only
+  // the roles that form global addresses from the plan's records check it,
+  // each at its first record (where it waits for that record anyway): the
+  // producers (block-table reads), the appended rows and the softmax
+  // (output writes).  A producer that finds a plan made for other arguments
+  // reports it and raises the abort flag, which ends the other roles.
+  const int32_t seg_stamp =
+      plan_stamp(prm.batch, prm.max_ranges, kTile, prm.block_size, prm.max_blocks_per_seq);
+  auto plan_ok = [&]() {
+    return plan_record_ok(seg_n, seg_first, seg_stamp, prm.batch,
+                          prm.max_blocks_per_seq * prm.block_size, 2 * prm.max_ranges);
+  };
   const int own0 = half * 4;        // first own 64-dim chunk (of the 8 kv_c chunks)
   const int oth0 = (1 - half) * 4;  // first other chunk
   const int BS = prm.block_size;
@@ -291,6 +303,13 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
     // ------------------------------------------------------------ TMA producers
     if (active && elect_one_sync()) {
       const bool own_role = (warp == 0);
+      // the plan's records address the block table: a plan made for other
+      // arguments stops both producers here, and the abort flag the others
+      const bool plan_good = plan_ok();
+      if (!plan_good) {
+        s.abort = 1;
+        report(prm.dev_status, MLA_ERR_DEVICE_PLAN);
+      }
       // normal priority: the pair's other CTA reads every tile too, usually a
       // little later; evict-first lines were often gone by then (ncu: ~19%
       // extra DRAM reads on a 64 x 4096 layer)
@@ -331,14 +350,14 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
         }
         fc_t += kTile;
       };
-      load_next();
+      if (plan_good) load_next();
       if (own_role) {
         prefetch_tmap(&maps.kv4);
       } else {
         prefetch_tmap(&maps.kv5);
         prefetch_tmap(&maps.kv1);
       }
-      bool ok = true;
+      bool ok = plan_good;
       while (ok && it.next(t0, t1, slot_p)) {
         for (int32_t tt = t0; tt < t1; tt += kTile, ++g) {
           // cache rows of the tile's boxes (one box per page, or one per tile):
@@ -432,7 +451,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
           }
         }
       }
-      if (s.abort) {
+      if (s.abort && plan_good) {
         // the consumers gave up: let the last issued loads land before exit
         for (int i = 0; i < kSlots; ++i) {
           uint64_t *landed = kFp8 ? (own_role ? &s.own_staged[i] : &s.other_staged[i])
@@ -654,7 +673,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
       // the first segment's Q (its waits pass at once)
       if (leader && qi.next(qt0, qt1, qslot)) qok = load_q();
       __syncwarp();
-      if (prm.kv_new) {
+      if (prm.kv_new && plan_ok()) {  // the rows' slots come from the plan's records
         SegIter<kTile> it;
         it.init(v, prm.batch, pair, seg_n, seg_first);
         int32_t t0, t1, slot_p;
@@ -767,7 +786,7 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
       if (prm.lse && half == 0) prm.lse[(int64_t)b * kHeads + h] = -INFINITY;
     }
 
-    if (active) {
+    if (active && plan_ok()) {  // outputs are written where the plan's records say
       SegIter<kTile> it;
       it.init(v, prm.batch, pair, seg_n, seg_first);
       int32_t t0, t1, slot_p;

@@ -226,12 +226,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
   const bool active = seg_n > 0;
+  // Whether the plan was made for these arguments (see plan_record_ok),
+  // checked by the roles that form global addresses from its records, at
+  // their first record: the tile producer (block-table reads; it reports a
+  // plan made for other arguments and raises the abort flag, which ends the
+  // other roles) and the softmax (output writes).
+  const int32_t seg_stamp =
+      plan_stamp(prm.batch, prm.max_ranges, kTile, prm.block_size, prm.max_blocks_per_seq);
+  auto plan_ok = [&]() {
+    return plan_record_ok(seg_n, seg_first, seg_stamp, prm.batch,
+                          prm.max_blocks_per_seq * prm.block_size, 2 * prm.max_ranges);
+  };
   const int BS = prm.block_size;
   const bool big_pages = BS >= kTile;  // a tile lies inside one page: one box
 
   if (warp == 0) {
     // ------------------------------------------------------------ tile loads
     if (active && elect_one_sync()) {
+      const bool plan_good = plan_ok();
+      if (!plan_good) {
+        s.abort = 1;
+        report(prm.dev_status, MLA_ERR_DEVICE_PLAN);
+      }
       SegIter<kTile> it;
       it.init(v, prm.batch, range, seg_n, seg_first);
       int32_t t0, t1, slot_p;
@@ -245,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         prefetch_tmap(&maps.kv2d);
       }
-      bool ok = true;
+      bool ok = plan_good;
       while (ok && it.next(t0, t1, slot_p)) {
         const int32_t *row = prm.block_table + (int64_t)it.b * prm.max_blocks_per_seq;
         for (int32_t tt = t0; tt < t1; tt += kTile, ++g) {
@@ -493,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (prm.lse && st < H) prm.lse[(int64_t)b * H + st] = -INFINITY;
     }
 
-    if (active) {
+    if (active && plan_ok()) {  // outputs are written where the plan's records say
       SegIter<kTile> it;
       it.init(v, prm.batch, range, seg_n, seg_first);
       int32_t t0, t1, slot_p;

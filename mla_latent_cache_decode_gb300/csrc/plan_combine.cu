@@ -203,6 +203,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
   // the first kSegCache segments of every range (see SegRec)
   int32_t *seg_count = const_cast<int32_t *>(v.seg_count);
   SegRec *seg_rec = const_cast<SegRec *>(v.seg_rec);
+  const int32_t stamp =
+      plan_stamp(batch, max_ranges, unit_tokens, block_size, max_blocks_per_seq);
   for (int p = tid; p < max_ranges; p += kPlanThreads) {
     int32_t n = 0;
     if (p < P) {
@@ -223,7 +225,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
                 block_table[(int64_t)b * max_blocks_per_seq + r.t0 / block_size];
             if (blk >= 0 && (int64_t)blk < num_blocks) r.row0 = blk * block_size + r.t0 % block_size;
           }
-          r.pad0 = r.pad1 = r.pad2 = 0;
+          r.stamp = stamp;
+          r.pad1 = r.pad2 = 0;
           seg_rec[(int64_t)p * kSegCache + n] = r;
         }
         ++n;
@@ -352,6 +355,9 @@ __global__ void __launch_bounds__(kHeads) plan_combine_kernel(void *ws, int32_t 
   const int h = blockIdx.z * kBlockHeads + hb;
   const ReqSplit rs = v.req_split[b];
   if (rs.p0 == rs.p1) return;  // not split (or empty): the decode wrote it
+  // a plan made for other arguments (the decode reports it): stay inside the
+  // partials' slots whatever the record holds
+  if (rs.p0 < 0 || rs.p0 > rs.p1 || rs.p1 >= max_ranges) return;
   const int nsplit = rs.p1 - rs.p0 + 1;
   auto slot_of_split = [&](int k) -> int64_t {
     return k == 0 ? 2 * rs.p0 + rs.first_odd : 2 * (rs.p0 + k);
@@ -506,6 +512,9 @@ __global__ void __launch_bounds__(kTpCombThreads) tp_combine_kernel(void *ws, in
   const int b = blockIdx.x, h = blockIdx.y, t = threadIdx.x;
   const ReqSplit rs = v.req_split[b];
   if (rs.p0 == rs.p1) return;  // not split (or empty): the decode wrote it
+  // a plan made for other arguments (the decode reports it): stay inside the
+  // partials' slots whatever the record holds
+  if (rs.p0 < 0 || rs.p0 > rs.p1 || rs.p1 >= max_ranges) return;
   const int nsplit = rs.p1 - rs.p0 + 1;
   auto slot_of_split = [&](int k) -> int64_t {
     return k == 0 ? 2 * rs.p0 + rs.first_odd : 2 * (rs.p0 + k);

@@ -41,9 +41,10 @@ def test_binding_names_match_header():
 def test_status_strings_and_version(lib):
     lib.mla_status_string.restype = ctypes.c_char_p
     lib.mla_abi_version.restype = ctypes.c_int
-    assert lib.mla_abi_version() == 3
-    names = [lib.mla_status_string(i).decode() for i in range(7)]
+    assert lib.mla_abi_version() == 4
+    names = [lib.mla_status_string(i).decode() for i in range(8)]
     assert names[0] == "MLA_OK" and names[6] == "MLA_ERR_DEVICE_TIMEOUT"
+    assert names[7] == "MLA_ERR_DEVICE_PLAN"
     assert lib.mla_status_string(99).decode() == "MLA_ERR_UNKNOWN"
 
 

@@ -838,3 +838,51 @@ def test_fewer_heads_against_oracle(mla, heads, planned):
                                  np.array(lens, np.int32), dl["softmax_scale"])
     assert_close(host_f64(out), ref, f"{heads} heads")
     assert_lse_close(lse.cpu().numpy(), ref_lse)
+
+
+# ------------------------------------------------------------ a plan made for other arguments
+
+@pytest.mark.parametrize("case", ["unplanned", "other_heads", "other_batch", "other_page"])
+def test_mismatched_plan_is_reported(mla, case):
+    """mla_decode_planned with a workspace whose plan was made for other
+    arguments (or never made) reports MLA_ERR_DEVICE_PLAN: the decode checks
+    the plan's header before reading it, and the combine stays within the
+    workspace.  A correctly planned call on the same workspace then gives the
+    oracle's result."""
+    lens = [300, 1000, 77, 2048]
+    w = mi.custom_workload(lens, block_size=64, append=False, pool_factor=1.5)
+    heads = 16 if case == "other_heads" else 128
+    dl = mi.make_device_layer(w, 0, "cuda", q_kind="sharp", num_heads=heads)
+    B = len(lens)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.full((max(mla.mla_decode_workspace_size(B, 128), mla.mla_decode_workspace_size(B, 16),
+                         mla.mla_decode_workspace_size(B + 1, 128)),), 0x5A, dtype=torch.uint8,
+                    device="cuda")   # never planned: a byte pattern
+    if case == "other_heads":     # planned for 128 heads, decoded with 16
+        mla.mla_decode_plan(dl["seq_lens"], dl["block_table"], 64, ws, num_heads=128,
+                            dev_status=status)
+    elif case == "other_batch":   # planned for one more request
+        sl = torch.cat([dl["seq_lens"], dl["seq_lens"][:1]])
+        bt = torch.cat([dl["block_table"], dl["block_table"][:1]])
+        mla.mla_decode_plan(sl, bt, 64, ws, dev_status=status)
+    elif case == "other_page":    # the same rows seen as pages of 32
+        bt32 = torch.repeat_interleave(dl["block_table"], 2, dim=1)
+        mla.mla_decode_plan(dl["seq_lens"], bt32, 32, ws, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    out = torch.full((B, heads, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, heads), float("nan"), dtype=torch.float32, device="cuda")
+    args = (dl["q"], dl["cache"], dl["block_table"], dl["seq_lens"], dl["softmax_scale"], out, lse)
+    mla.mla_decode_planned(*args, workspace=ws, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 7   # MLA_ERR_DEVICE_PLAN
+    status.zero_()
+    mla.mla_decode_plan(dl["seq_lens"], dl["block_table"], 64, ws, num_heads=heads,
+                        dev_status=status)
+    mla.mla_decode_planned(*args, workspace=ws, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref, ref_lse = oracle.decode(host_bits(dl["q"]), host_bits(dl["cache"]), dl["block_table_host"],
+                                 np.array(lens, np.int32), dl["softmax_scale"])
+    assert_close(host_f64(out), ref, case)
+    assert_lse_close(lse.cpu().numpy(), ref_lse)
