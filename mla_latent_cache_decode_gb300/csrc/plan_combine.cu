@@ -8,6 +8,7 @@
 // one long request does not stall the batch [dp-attention-expert-parallel-mla-
 // kv-replication (inferenceinterviews.com), "What it costs"].
 #include "common.cuh"
+#include "merge.cuh"
 
 namespace mla {
 
@@ -339,8 +340,6 @@ __device__ __forceinline__ void combine_row(const float *__restrict__ o_part,
 // sum, 16 weighted dims) are then merged through shared memory, each thread
 // finishing 16 / kLanes dims of one head.  The bf16 results leave as 32-byte
 // row pieces.  grid = (batch, 512 / 16, kLanes), 128 threads.
-constexpr int kCombDims = 16;
-constexpr int kCombGroup = 4;  // splits per lane whose loads are in flight together
 
 template <int kLanes>
 __global__ void __launch_bounds__(kHeads) plan_combine_kernel(void *ws, int32_t batch,
@@ -355,73 +354,14 @@ __global__ void __launch_bounds__(kHeads) plan_combine_kernel(void *ws, int32_t 
   const int h = blockIdx.z * kBlockHeads + hb;
   const ReqSplit rs = v.req_split[b];
   if (rs.p0 == rs.p1) return;  // not split (or empty): the decode wrote it
-  // a plan made for other arguments (the decode reports it): stay inside the
-  // partials' slots whatever the record holds
-  if (rs.p0 < 0 || rs.p0 > rs.p1 || rs.p1 >= max_ranges) return;
-  const int nsplit = rs.p1 - rs.p0 + 1;
-  auto slot_of_split = [&](int k) -> int64_t {
-    return k == 0 ? 2 * rs.p0 + rs.first_odd : 2 * (rs.p0 + k);
-  };
+  if (!split_in_bounds(rs, max_ranges)) return;
   __shared__ __align__(16) __nv_bfloat16 tile[kBlockHeads][kCombDims + 8];  // +8: stagger
   float4 acc[kCombDims / 4];
-#pragma unroll
-  for (int j = 0; j < kCombDims / 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-  float m = -INFINITY, z = 0.f;
-  // this lane's splits kCombGroup at a time; the running max rescales what
-  // was summed so far
-  for (int k0 = sl; k0 < nsplit; k0 += kLanes * kCombGroup) {
-    float l[kCombGroup];
-    float4 x[kCombGroup][kCombDims / 4];
-#pragma unroll
-    for (int u = 0; u < kCombGroup; ++u) {
-      const int k = k0 + u * kLanes;
-      const int64_t w = slot_of_split(k < nsplit ? k : k0);  // k0 < nsplit: a valid slot
-      l[u] = k < nsplit ? v.lse_part[w * kHeads + h] : -INFINITY;
-      const uint4 *src = reinterpret_cast<const uint4 *>(v.o_part) +
-                         (w * (kVDim / 8) + d0 / 8) * kHeads + h;
-#pragma unroll
-      for (int j = 0; j < kCombDims / 8; ++j) {
-        const uint4 raw = __ldg(src + (int64_t)j * kHeads);
-        x[u][2 * j] = make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u),
-                                  __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u));
-        x[u][2 * j + 1] = make_float4(__uint_as_float(raw.z << 16), __uint_as_float(raw.z & 0xffff0000u),
-                                      __uint_as_float(raw.w << 16), __uint_as_float(raw.w & 0xffff0000u));
-      }
-    }
-    float mc = m;
-#pragma unroll
-    for (int u = 0; u < kCombGroup; ++u) mc = fmaxf(mc, l[u]);
-    if (mc == -INFINITY) continue;
-    if (m != -INFINITY && mc != m) {
-      const float r = __expf(m - mc);
-      z *= r;
-#pragma unroll
-      for (int j = 0; j < kCombDims / 4; ++j) {
-        acc[j].x *= r; acc[j].y *= r; acc[j].z *= r; acc[j].w *= r;
-      }
-    }
-    m = mc;
-#pragma unroll
-    for (int u = 0; u < kCombGroup; ++u) {
-      const float a = l[u] == -INFINITY ? 0.f : __expf(l[u] - m);
-      z += a;
-#pragma unroll
-      for (int j = 0; j < kCombDims / 4; ++j) {
-        acc[j].x += a * x[u][j].x; acc[j].y += a * x[u][j].y;
-        acc[j].z += a * x[u][j].z; acc[j].w += a * x[u][j].w;
-      }
-    }
-  }
+  float m, z;
+  accumulate_splits<kLanes>(v, rs, sl, h, d0, acc, m, z);
   if constexpr (kLanes == 1) {
-    const float inv = z > 0.f ? 1.f / z : 0.f;
-#pragma unroll
-    for (int j = 0; j < kCombDims / 4; ++j) {
-      *reinterpret_cast<__nv_bfloat162 *>(&tile[hb][4 * j]) =
-          __floats2bfloat162_rn(acc[j].x * inv, acc[j].y * inv);
-      *reinterpret_cast<__nv_bfloat162 *>(&tile[hb][4 * j + 2]) =
-          __floats2bfloat162_rn(acc[j].z * inv, acc[j].w * inv);
-    }
-    if (lse && blockIdx.y == 0) lse[(int64_t)b * kHeads + h] = z > 0.f ? m + logf(z) : -INFINITY;
+    const float lse_h = finish_row16(acc, m, z, &tile[hb][0]);
+    if (lse && blockIdx.y == 0) lse[(int64_t)b * kHeads + h] = lse_h;
   } else {
     constexpr int kDimsPerThread = kCombDims / kLanes;
     __shared__ float s_m[kLanes][kBlockHeads], s_z[kLanes][kBlockHeads];

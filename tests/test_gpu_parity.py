@@ -437,9 +437,13 @@ def test_config2_layer_repeated_bit_identical(mla):
             assert torch.equal(out.view(torch.int16), first.view(torch.int16)), f"run {rep} differs"
 
 
-def test_partial_then_combine_equals_planned(mla):
-    """mla_decode_partial + mla_combine_planned is exactly mla_decode_planned."""
-    w = mi.workload(4)
+@pytest.mark.parametrize("cfg", [4, 2])
+def test_partial_then_combine_equals_planned(mla, cfg):
+    """mla_decode_partial + mla_combine_planned is exactly mla_decode_planned:
+    on config 4 (8 requests) the planned form also runs the separate combine,
+    on config 2 (64 requests) it merges inside the decode kernel, with the
+    same arithmetic."""
+    w = mi.workload(cfg)
     dl, host = _device_layer_and_host(w, 0, "sharp")
     ws = mla.make_workspace(w.batch)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -608,12 +612,15 @@ def test_config3_dp_rank_61_layers_sampled(mla):
     assert int(status.item()) == 0
 
 
-def test_graph_captured_step_equals_eager(mla):
+@pytest.mark.parametrize("lens", [[700, 64, 1500, 33, 4096, 129],
+                                  [700, 64, 1500, 33, 4096, 129, 2000, 517, 3000, 90] * 4])
+def test_graph_captured_step_equals_eager(mla, lens):
     """A step captured in a CUDA graph (plan + per-layer fused append and
     decode, on a side stream, as the benchmark runs it) gives the same bits as
     the same calls run eagerly, replay after replay; its outputs match the
-    oracle on sampled requests."""
-    w = mi.custom_workload([700, 64, 1500, 33, 4096, 129], block_size=64, layers=2, append=True,
+    oracle on sampled requests.  Six requests keep the separate combine;
+    forty merge their splits inside the decode (a cooperative launch)."""
+    w = mi.custom_workload(lens, block_size=64, layers=2, append=True,
                            pool_factor=1.5, name="graph_check")
     bt = mi.make_block_table(mi.rng_for(w.config_id, 0, 1), w.seq_lens, w.block_size,
                              w.num_blocks())
