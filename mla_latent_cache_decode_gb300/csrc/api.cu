@@ -42,7 +42,8 @@ cudaError_t launch_decode_tc(const void *q, const void *cache, int64_t num_block
                              const int32_t *block_table, int32_t max_blocks_per_seq, int32_t batch,
                              float softmax_scale, void *out, float *lse, void *ws,
                              int32_t max_ranges, int32_t *dev_status, cudaStream_t stream,
-                             const void *kv_new = nullptr, bool fp8 = false, float kv_scale = 1.f);
+                             const void *kv_new = nullptr, bool fp8 = false, float kv_scale = 1.f,
+                             bool early_launch = false);
 
 namespace {
 
@@ -70,6 +71,22 @@ int max_ranges_current() { return tc_max_pairs(); }
 // A tensor-parallel rank's few heads (1 to 32) run on their own kernel
 // (decode_tp.cu), whose plan has one range per SM.
 bool few_heads(int32_t num_heads) { return num_heads >= 1 && num_heads <= tp_max_heads(); }
+
+// The 128-head bf16 decode is launched as a programmatic dependent (its setup
+// may overlap the previous kernel's tail; see decode_tc.cu) when the split
+// combine of the same batch, which releases its dependents at entry, runs in
+// one wave of 128-thread blocks: early decode CTAs would otherwise hold SMs
+// that the combine's later waves need (measured slower on 256 requests).
+// The FP8 decode measured slower launched early and is not.
+bool decode_launches_early(int32_t batch) {
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return false;
+  const int64_t r = max_ranges_current();
+  const int64_t lanes = (int64_t)batch * 8 <= r ? 16 : ((int64_t)batch * 4 <= r ? 4 : 1);
+  return (int64_t)batch * (kVDim / 16) * lanes <= 16 * (int64_t)sms;
+}
 
 // 33 to 127 heads: the workspace holds q padded to 128 heads and the padded
 // output and lse, behind the plan and partials.  The pad heads hold whatever the workspace held:
@@ -260,7 +277,8 @@ mla_status_t mla_decode_partial(const void *q, void *cache, const void *kv_new,
   }
   cudaError_t e = launch_decode_tc(q, cache, num_blocks, block_size, block_table,
                                    max_blocks_per_seq, batch, softmax_scale, out, lse, workspace,
-                                   max_ranges_current(), dev_status, (cudaStream_t)stream, kv_new);
+                                   max_ranges_current(), dev_status, (cudaStream_t)stream, kv_new,
+                                   false, 1.f, decode_launches_early(batch));
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "decode launch");
 }
 

@@ -145,6 +145,7 @@ struct Params {
   uint4 *cache_rows;    // the cache, for those stores
   float kv_scale;       // FP8 cache: the value of a code is value(code) * kv_scale
   float kv_inv_scale;   // FP8 cache: a new row is stored as code(x * kv_inv_scale)
+  int32_t early_launch; // launched as a programmatic dependent (see griddep_wait below)
 };
 
 __device__ __forceinline__ void set_abort(Smem &s, int32_t *dev_status) {
@@ -235,10 +236,19 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
   const int pair = blockIdx.x >> 1;
   const PlanView v = plan_view(prm.ws, prm.batch, kHeads, prm.max_ranges);
   const volatile int *abort_flag = &s.abort;
-  // this range's segment count and first segment record, requested before the
-  // setup below so that their latency overlaps it
-  const int32_t seg_n = v.seg_count[pair];
-  const SegRec seg_first = v.seg_rec[(int64_t)pair * kSegCache];
+  // This range's segment count and first segment record, requested before
+  // the setup below so that their latency overlaps it; launched early, only
+  // their lines are fetched into L2 now, and they are read once the previous
+  // kernel has completed (griddep_wait below).
+  int32_t seg_n = 0;
+  SegRec seg_first = {};
+  if (!prm.early_launch) {
+    seg_n = v.seg_count[pair];
+    seg_first = v.seg_rec[(int64_t)pair * kSegCache];
+  } else if (tid == 32) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(v.seg_count + pair) : "memory");
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(v.seg_rec + (int64_t)pair * kSegCache) : "memory");
+  }
 
   if (tid == 0) {
     for (int i = 0; i < kSlots; ++i) {
@@ -280,6 +290,15 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
+  // Launched as a programmatic dependent (after a one-wave combine), the
+  // setup above ran during the previous kernel's tail; everything below —
+  // the plan, q, the cache, the outputs, the partials — waits for it to
+  // complete and for its writes to be visible.
+  griddep_wait();
+  if (prm.early_launch) {
+    seg_n = v.seg_count[pair];
+    seg_first = v.seg_rec[(int64_t)pair * kSegCache];
+  }
 
   const bool active = seg_n > 0;  // ranges past the plan's count have none
   // Whether the plan was made for these arguments (see plan_record_ok).  Only
@@ -1126,7 +1145,7 @@ cudaError_t launch_decode_tc(const void *q, const void *cache, int64_t num_block
                              const int32_t *block_table, int32_t max_blocks_per_seq, int32_t batch,
                              float softmax_scale, void *out, float *lse, void *ws,
                              int32_t max_ranges, int32_t *dev_status, cudaStream_t stream,
-                             const void *kv_new, bool fp8, float kv_scale) {
+                             const void *kv_new, bool fp8, float kv_scale, bool early_launch) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -1156,11 +1175,19 @@ cudaError_t launch_decode_tc(const void *q, const void *cache, int64_t num_block
   p.dev_status = dev_status;
   p.kv_new = (const uint4 *)kv_new;
   p.cache_rows = (uint4 *)const_cast<void *>(cache);
-  if (fp8)
-    tc::decode_tc_kernel<true><<<2 * max_ranges, tc::kThreadsFp8, smem, stream>>>(maps, p);
-  else
-    tc::decode_tc_kernel<false><<<2 * max_ranges, tc::kThreads, smem, stream>>>(maps, p);
-  return cudaGetLastError();
+  p.early_launch = early_launch ? 1 : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * max_ranges);
+  cfg.blockDim = dim3(fp8 ? tc::kThreadsFp8 : tc::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = early_launch ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return fp8 ? cudaLaunchKernelEx(&cfg, tc::decode_tc_kernel<true>, maps, p)
+             : cudaLaunchKernelEx(&cfg, tc::decode_tc_kernel<false>, maps, p);
 }
 
 }  // namespace mla

@@ -21,7 +21,8 @@ cudaError_t launch_decode_tc(const void *q, const void *cache, int64_t num_block
                              const int32_t *block_table, int32_t max_blocks_per_seq, int32_t batch,
                              float softmax_scale, void *out, float *lse, void *ws,
                              int32_t max_ranges, int32_t *dev_status, cudaStream_t stream,
-                             const void *kv_new = nullptr, bool fp8 = false, float kv_scale = 1.f);
+                             const void *kv_new = nullptr, bool fp8 = false, float kv_scale = 1.f,
+                             bool early_launch = false);
 mla_status_t noalloc_fail(mla_status_t s, const char *msg);
 }  // namespace mla
 

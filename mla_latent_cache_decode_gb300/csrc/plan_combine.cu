@@ -9,6 +9,7 @@
 // kv-replication (inferenceinterviews.com), "What it costs"].
 #include "common.cuh"
 #include "merge.cuh"
+#include "sm100.cuh"
 
 namespace mla {
 
@@ -347,6 +348,9 @@ __global__ void __launch_bounds__(kHeads) plan_combine_kernel(void *ws, int32_t 
                                                               __nv_bfloat16 *__restrict__ out,
                                                               float *__restrict__ lse) {
   constexpr int kBlockHeads = kHeads / kLanes;
+  // the next layer's decode may launch its prologue meanwhile (it waits for
+  // this grid before it reads or writes anything this one touches)
+  sm100::griddep_launch_dependents();
   PlanView v = plan_view(ws, batch, kHeads, max_ranges);
   const int b = blockIdx.x, d0 = blockIdx.y * kCombDims;
   const int sl = (int)threadIdx.x / kBlockHeads;  // split lane

@@ -83,6 +83,19 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+
+// The next kernel in the stream, if launched as a programmatic dependent,
+// may start now (once every CTA of this grid has triggered or exited).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Returns once the grids this one depends on have completed and their memory
+// operations are visible (at once when not launched as a dependent).
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m) {
