@@ -294,6 +294,29 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
   // setup above ran during the previous kernel's tail; everything below —
   // the plan, q, the cache, the outputs, the partials — waits for it to
   // complete and for its writes to be visible.
+  if (!kFp8 && prm.early_launch && (warp == 0 || warp == 3 || warp == 9) && lane == 0) {
+    // While the previous kernel ends: the first tile's parts and the first
+    // request's q towards L2, at the places the plan's first record names.
+    // Read before the wait, that record may be stale: it only aims these
+    // prefetches (out-of-range boxes fetch nothing), and everything is read
+    // again after the wait.
+    const int32_t n0 = v.seg_count[pair];
+    const SegRec r0 = v.seg_rec[(int64_t)pair * kSegCache];
+    if (n0 <= 0 || r0.b < 0 || r0.b >= prm.batch) {
+      // nothing to aim at
+    } else if (warp == 9) {
+      for (int c = 0; c < kRow / 64; ++c) tma_prefetch_2d(&maps.q, 64 * c, r0.b * kHeads);
+    } else if (r0.row0 >= 0 && prm.block_size >= kTile) {
+      if (warp == 0) {
+        tma_prefetch_3d(&maps.kv4, 0, r0.row0, half * 4);
+      } else if (half == 0) {
+        tma_prefetch_3d(&maps.kv5, 0, r0.row0, 4);
+      } else {
+        tma_prefetch_3d(&maps.kv4, 0, r0.row0, 0);
+        tma_prefetch_3d(&maps.kv1, 0, r0.row0, 8);
+      }
+    }
+  }
   griddep_wait();
   if (prm.early_launch) {
     seg_n = v.seg_count[pair];
