@@ -13,8 +13,14 @@
 
 namespace mla {
 
-constexpr int kPlanThreads = 1024;
+// The planner is one block whose phases are short dependent chains between
+// barriers; every warp issues every phase, so it runs 8 warps (2 per SM
+// sub-partition) rather than 32 and loops where a batch or the ranges exceed
+// a pass.
+constexpr int kPlanThreads = 256;
+constexpr int kPlanWarps = kPlanThreads / 32;
 constexpr int kMaxPlanRanges = 1024;  // boundaries are settled in shared memory
+constexpr int kPlanChunks = (kMaxPlanRanges + 1 + 31) / 32;  // 32-boundary chunks
 // Batches up to this size keep their prefixes and lengths in shared memory
 // too, so the planner's binary searches and walks make no global round trips
 // (larger batches read them back from the workspace).
@@ -34,8 +40,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
   int32_t *range_start = const_cast<int32_t *>(v.range_start);
   int32_t *range_first = const_cast<int32_t *>(v.range_first);
   int64_t *cost_prefix = const_cast<int64_t *>(v.cost_prefix);
-  __shared__ int64_t warp_sums[kPlanThreads / 32];
+  __shared__ int64_t warp_sums[kPlanWarps];
   __shared__ int64_t carry;
+  __shared__ int32_t chunk_ext[kPlanChunks];
   __shared__ int32_t bound[kMaxPlanRanges + 1];
   __shared__ int32_t s_rfirst[kMaxPlanRanges];
   __shared__ int32_t s_prefix[kPlanSmemBatch + 1], s_seq[kPlanSmemBatch];
@@ -77,13 +84,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
     if (lane == 31) warp_sums[wid] = x;
     __syncthreads();
     if (wid == 0) {
-      int64_t s = warp_sums[lane];
+      int64_t s = lane < kPlanWarps ? warp_sums[lane] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int64_t y = __shfl_up_sync(0xffffffffu, s, o);
         if (lane >= o) s += y;
       }
-      warp_sums[lane] = s;  // inclusive over warps
+      if (lane < kPlanWarps) warp_sums[lane] = s;  // inclusive over warps
     }
     __syncthreads();
     const int64_t incl = x + (wid > 0 ? warp_sums[wid - 1] : 0) + carry;
@@ -136,37 +143,58 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
   __syncthreads();
   // ... then the least change that makes them strictly increasing with
   // R_0 = 0 and R_P = U: R_p = p + min over q >= p of (max over q' <= q of
-  // (R_q' - q')), the last term pinned to U - P.  One warp, 32 at a time.
-  if (wid == 0 && P > 0) {
-    int32_t run = INT32_MIN;
-    for (int base = 0; base <= P; base += 32) {
-      const int p = base + lane;
+  // (R_q' - q')), the last term pinned to U - P.  R_0 = 0 and R_P = U hold
+  // already; when every range also got a unit (R_p - p non-decreasing, the
+  // usual case) the scans would change nothing.  Otherwise both run over
+  // chunks of 32 boundaries, one chunk a warp, and then take the other
+  // chunks' extremes in.
+  bool rising = true;
+  for (int p = tid; p < P; p += kPlanThreads) rising = rising && bound[p] <= bound[p + 1];
+  const bool fix = !__syncthreads_and(rising);
+  const int nch = (P + 1 + 31) / 32;
+  if (!fix) {
+    for (int p = tid; p <= P; p += kPlanThreads) bound[p] += p;
+  } else if (P > 0) {
+    for (int ch = wid; ch < nch; ch += kPlanWarps) {  // prefix max within chunks
+      const int p = ch * 32 + lane;
       int32_t x = p <= P ? bound[p] : INT32_MIN;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x = max(x, y);
       }
-      x = max(x, run);
       if (p <= P) bound[p] = x;
-      run = __shfl_sync(0xffffffffu, x, 31);
+      if (lane == 31) chunk_ext[ch] = x;
     }
-    __syncwarp();
-    if (lane == 0) bound[P] = U - P;
-    __syncwarp();
-    run = INT32_MAX;
-    for (int top = P; top >= 0; top -= 32) {
-      const int p = top - lane;
+    __syncthreads();
+    for (int ch = wid; ch < nch; ch += kPlanWarps) {  // ... and over the chunks before
+      int32_t c = INT32_MIN;
+      for (int k = lane; k < ch; k += 32) c = max(c, chunk_ext[k]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) c = max(c, __shfl_xor_sync(0xffffffffu, c, o));
+      const int p = ch * 32 + lane;
+      if (p <= P) bound[p] = p == P ? U - P : max(bound[p], c);
+    }
+    __syncthreads();
+    for (int ch = wid; ch < nch; ch += kPlanWarps) {  // suffix min within chunks (from the top)
+      const int p = P - (ch * 32 + lane);
       int32_t x = p >= 0 ? bound[p] : INT32_MAX;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x = min(x, y);
       }
-      x = min(x, run);
-      run = __shfl_sync(0xffffffffu, x, 31);
-      __syncwarp();
-      if (p >= 0) bound[p] = x + p;
+      if (p >= 0) bound[p] = x;
+      if (lane == 31) chunk_ext[ch] = x;
+    }
+    __syncthreads();
+    for (int ch = wid; ch < nch; ch += kPlanWarps) {  // ... and over the chunks above
+      int32_t c = INT32_MAX;
+      for (int k = lane; k < ch; k += 32) c = min(c, chunk_ext[k]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) c = min(c, __shfl_xor_sync(0xffffffffu, c, o));
+      const int p = P - (ch * 32 + lane);
+      if (p >= 0) bound[p] = min(bound[p], c) + p;
     }
   }
   __syncthreads();
@@ -180,9 +208,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
       if (pre[mid] <= r) lo = mid; else hi = mid - 1;
     }
     range_first[p] = lo;
-    s_rfirst[p] = lo;
+    s_rfirst[p] = lo;  // read below by this thread only (the same p)
   }
-  __syncthreads();  // range_first, prefix and the clamped lengths are visible to the block
   // every request's split, for the combine (see ReqSplit)
   auto range_of = [&](int32_t u) {  // the largest p < P with R_p <= u
     int lo = 0, hi = P - 1;
@@ -192,8 +219,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
     }
     return lo;
   };
+  // (requests from the block's last thread down, so that a small batch's
+  // splits and the ranges' records below go to different warps)
   ReqSplit *req_split = const_cast<ReqSplit *>(v.req_split);
-  for (int b = tid; b < batch; b += kPlanThreads) {
+  for (int b = kPlanThreads - 1 - tid; b < batch; b += kPlanThreads) {
     const int32_t Ub = pre[b], n = pre[b + 1] - Ub;
     ReqSplit r;
     r.p0 = n > 0 ? range_of(Ub) : 0;
@@ -207,32 +236,47 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
   SegRec *seg_rec = const_cast<SegRec *>(v.seg_rec);
   const int32_t stamp =
       plan_stamp(batch, max_ranges, unit_tokens, block_size, max_blocks_per_seq);
+  const bool rows = block_table && block_size >= unit_tokens;
   for (int p = tid; p < max_ranges; p += kPlanThreads) {
     int32_t n = 0;
     if (p < P) {
       const int32_t r0 = bound[p], r1 = bound[p + 1];
-      for (int b = s_rfirst[p]; b < batch && pre[b] < r1; ++b) {
-        const int32_t Ub = pre[b], Ue = pre[b + 1];
-        const int32_t u0 = max(r0, Ub), u1 = min(r1, Ue);
-        if (u0 >= u1) continue;
-        if (n < kSegCache) {
-          SegRec r;
-          r.b = b;
-          r.t0 = (u0 - Ub) * unit_tokens;
-          r.t1 = min((u1 - Ub) * unit_tokens, sq[b]);
-          r.slot = segment_slot(p, r0, r1, Ub, Ue);
-          r.row0 = -1;
-          if (block_table && block_size >= unit_tokens && r.t0 < r.t1) {
-            const int32_t blk =
-                block_table[(int64_t)b * max_blocks_per_seq + r.t0 / block_size];
-            if (blk >= 0 && (int64_t)blk < num_blocks) r.row0 = blk * block_size + r.t0 % block_size;
-          }
+      // the first kSegCache segments, their table entries loaded together
+      int b = s_rfirst[p];
+      SegRec rec[kSegCache];
+      int32_t blk[kSegCache];
+#pragma unroll
+      for (int i = 0; i < kSegCache; ++i) {
+        while (b < batch && pre[b] < r1 && pre[b + 1] <= max(r0, pre[b])) ++b;  // empty ones
+        blk[i] = -1;
+        if (b < batch && pre[b] < r1) {
+          const int32_t Ub = pre[b], Ue = pre[b + 1];
+          const int32_t u0 = max(r0, Ub), u1 = min(r1, Ue);
+          rec[i].b = b;
+          rec[i].t0 = (u0 - Ub) * unit_tokens;
+          rec[i].t1 = min((u1 - Ub) * unit_tokens, sq[b]);
+          rec[i].slot = segment_slot(p, r0, r1, Ub, Ue);
+          if (rows && rec[i].t0 < rec[i].t1)
+            blk[i] = block_table[(int64_t)b * max_blocks_per_seq + rec[i].t0 / block_size];
+          ++n;
+          ++b;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kSegCache; ++i) {
+        if (i < n) {
+          SegRec r = rec[i];
+          r.row0 = blk[i] >= 0 && (int64_t)blk[i] < num_blocks
+                       ? blk[i] * block_size + r.t0 % block_size
+                       : -1;
           r.stamp = stamp;
           r.pad1 = r.pad2 = 0;
-          seg_rec[(int64_t)p * kSegCache + n] = r;
+          seg_rec[(int64_t)p * kSegCache + i] = r;
         }
-        ++n;
       }
+      // the count of the rest
+      for (; b < batch && pre[b] < r1; ++b)
+        if (min(r1, pre[b + 1]) > max(r0, pre[b])) ++n;
     }
     seg_count[p] = n;
   }
