@@ -706,7 +706,20 @@ def test_plan_invariants(mla, cfg):
     balanced: the targets are C/P apart and a boundary lands within a start's
     cost or a unit of its target, so no two ranges differ by more than
     2 x (7 + 2)."""
-    w = mi.workload(cfg)
+    _check_plan(mla, mi.workload(cfg))
+
+
+@pytest.mark.parametrize("lens", [[4864], [3000], [4864, 64, 1], [64] * 40 + [2560],
+                                  [1600, 1, 1, 1, 1, 1600, 1, 1, 1, 1, 1600]],
+                         ids=["76units", "47units", "76units+2", "40x1+40units", "3x25units+8x1"])
+def test_plan_invariants_crowded(mla, lens):
+    """Workloads with about as many units as split ranges, where the cost
+    targets leave some ranges empty and the planner's fix-up moves the
+    boundaries (over several 32-boundary chunks): the same invariants."""
+    _check_plan(mla, mi.custom_workload(lens, block_size=64, append=False, pool_factor=1.5))
+
+
+def _check_plan(mla, w):
     dl = mi.make_device_layer(w, 0, "cuda")
     ws = mla.make_workspace(w.batch)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -716,6 +729,7 @@ def test_plan_invariants(mla, cfg):
     assert int(status.item()) == 0
     pl = _read_plan(ws, w.batch)
     unit = 64
+    bt = dl["block_table"].cpu().numpy()
     seq = dl["seq_lens"].cpu().numpy().astype(np.int64)
     units = (seq + unit - 1) // unit
     assert np.array_equal(pl["seq"], seq)
@@ -737,6 +751,10 @@ def test_plan_invariants(mla, cfg):
         assert pl["segc"][p] == len(segs)
         for i, sgm in enumerate(segs[:4]):
             assert tuple(pl["recs"][p, i, :4]) == sgm, (p, i)
+            b, t0, t1 = sgm[0], sgm[1], sgm[2]
+            row0 = (int(bt[b, t0 // w.block_size]) * w.block_size + t0 % w.block_size
+                    if w.block_size >= unit and t0 < t1 else -1)
+            assert pl["recs"][p, i, 4] == row0, (p, i, "row0")
         cost.append(2 * (r1 - r0) + 7 * int(((starts >= r0) & (starts < r1)).sum()))
     for b in range(w.batch):
         if units[b] == 0:
