@@ -173,6 +173,15 @@ mla_status_t mla_decode_plan(const int32_t *seq_lens, const int32_t *block_table
  * units in int32); batch >= 0 (0 = no-op).  Else MLA_ERR_INVALID_ARGUMENT.
  * Rows the plan does not cover (tails past seq_len, unused blocks) are never
  * read, whatever they hold.
+ * Launch order: every launch is ordered after the previous work on `stream`
+ * as usual.  Some are programmatic dependents of the kernel before them (they
+ * set up while it ends and wait for it to complete before touching memory),
+ * and the 128-head decode releases its own programmatic dependents once its
+ * CTAs have requested their last tile, before its outputs are written.  A
+ * caller's kernel launched after these calls with programmatic stream
+ * serialization must therefore wait for the grid before it reads their
+ * outputs (griddepcontrol.wait), as the library's own kernels do; kernels
+ * launched without that attribute are unaffected.
  */
 mla_status_t mla_decode(const void *q, const void *cache, int64_t num_blocks, int32_t block_size,
                         const int32_t *block_table, int32_t max_blocks_per_seq,

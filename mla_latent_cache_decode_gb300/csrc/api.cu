@@ -21,7 +21,7 @@ cudaError_t launch_plan(const int32_t *seq_lens, const int32_t *block_table, int
                         int32_t block_size, int32_t max_ranges, void *ws, int32_t heads,
                         int32_t *dev_status, cudaStream_t stream);
 cudaError_t launch_plan_combine(void *ws, int32_t batch, int32_t heads, int32_t max_ranges,
-                                void *out, float *lse, cudaStream_t stream);
+                                void *out, float *lse, cudaStream_t stream, bool early);
 cudaError_t launch_offsets_combine(const float *o_part, const float *lse_part,
                                    const int32_t *offsets, int32_t batch, int32_t heads, void *out,
                                    float *lse, cudaStream_t stream);
@@ -78,6 +78,13 @@ bool few_heads(int32_t num_heads) { return num_heads >= 1 && num_heads <= tp_max
 // one wave of 128-thread blocks: early decode CTAs would otherwise hold SMs
 // that the combine's later waves need (measured slower on 256 requests).
 // The FP8 decode measured slower launched early and is not.
+//
+// The split combine is launched as a programmatic dependent of the decode
+// when that decode was not launched early itself (a larger batch, or an FP8
+// cache): its blocks then take the SMs that decode CTAs free and wait there
+// for the whole decode.  After an early-launched decode that was slower
+// (config 3: 2.088 against 2.042 ms), likely because the combine's one wave
+// crowded onto the first SMs freed.
 bool decode_launches_early(int32_t batch) {
   int sms = 0, dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -323,7 +330,7 @@ mla_status_t mla_combine_planned(void *workspace, size_t workspace_bytes, int32_
       few ? launch_tp_combine(workspace, batch, num_heads, tp_max_ranges(), out, lse,
                               (cudaStream_t)stream)
           : launch_plan_combine(workspace, batch, num_heads, max_ranges_current(), out, lse,
-                                (cudaStream_t)stream);
+                                (cudaStream_t)stream, !decode_launches_early(batch));
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "combine launch");
 }
 
@@ -456,7 +463,7 @@ mla_status_t mla_decode_fp8_planned(const void *q, void *cache8, const void *kv_
                                    max_blocks_per_seq, batch, softmax_scale, out, lse, workspace,
                                    max_ranges_current(), dev_status, st, kv_new, true, kv_scale);
   if (e != cudaSuccess) return cuda_fail(e, "FP8 decode launch");
-  e = launch_plan_combine(workspace, batch, num_heads, max_ranges_current(), out, lse, st);
+  e = launch_plan_combine(workspace, batch, num_heads, max_ranges_current(), out, lse, st, true);
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "combine launch");
 }
 

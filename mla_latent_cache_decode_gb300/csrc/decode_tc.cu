@@ -493,6 +493,10 @@ __global__ void __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
           }
         }
       }
+      // every tile requested: a split combine launched as a programmatic
+      // dependent may start its blocks on SMs this grid frees (it waits for
+      // the whole grid before it reads anything)
+      if (own_role) griddep_launch_dependents();
       if (s.abort && plan_good) {
         // the consumers gave up: let the last issued loads land before exit
         for (int i = 0; i < kSlots; ++i) {

@@ -14,7 +14,7 @@ cudaError_t launch_plan(const int32_t *seq_lens, const int32_t *block_table, int
                         int32_t block_size, int32_t max_ranges, void *ws, int32_t heads,
                         int32_t *dev_status, cudaStream_t stream);
 cudaError_t launch_plan_combine(void *ws, int32_t batch, int32_t heads, int32_t max_ranges,
-                                void *out, float *lse, cudaStream_t stream);
+                                void *out, float *lse, cudaStream_t stream, bool early);
 int tc_unit_tokens();
 int tc_max_pairs();
 cudaError_t launch_decode_tc(const void *q, const void *cache, int64_t num_blocks, int32_t block_size,
@@ -148,7 +148,8 @@ extern "C" mla_status_t mla_decode_noalloc(const void *q, const void *cache, int
   if (e == cudaSuccess)
     e = launch_decode_tc(q, cache, num_blocks, block_size, block_table, max_blocks_per_seq, batch,
                          softmax_scale, out, lse, ws, ranges, dev_status, st);
-  if (e == cudaSuccess) e = launch_plan_combine(ws, batch, num_heads, ranges, out, lse, st);
+  // the decode above is not a programmatic dependent, so its combine is one
+  if (e == cudaSuccess) e = launch_plan_combine(ws, batch, num_heads, ranges, out, lse, st, true);
   if (e != cudaSuccess) return noalloc_fail(MLA_ERR_CUDA, cudaGetErrorString(e));
   return MLA_OK;
 }

@@ -395,6 +395,9 @@ __global__ void __launch_bounds__(kHeads) plan_combine_kernel(void *ws, int32_t 
   // the next layer's decode may launch its prologue meanwhile (it waits for
   // this grid before it reads or writes anything this one touches)
   sm100::griddep_launch_dependents();
+  // launched as a programmatic dependent of the decode, this block may start
+  // before the decode ends: the partials are read only once it has completed
+  sm100::griddep_wait();
   PlanView v = plan_view(ws, batch, kHeads, max_ranges);
   const int b = blockIdx.x, d0 = blockIdx.y * kCombDims;
   const int sl = (int)threadIdx.x / kBlockHeads;  // split lane
@@ -462,26 +465,31 @@ __global__ void __launch_bounds__(kHeads) plan_combine_kernel(void *ws, int32_t 
 }
 
 cudaError_t launch_plan_combine(void *ws, int32_t batch, int32_t heads, int32_t max_ranges,
-                                void *out, float *lse, cudaStream_t stream) {
+                                void *out, float *lse, cudaStream_t stream, bool early) {
   if (heads != kHeads) return cudaErrorInvalidValue;
   // Split lanes when requests average four or more ranges (a small batch,
   // where one long request may be spread over most of the SM pairs): 16 from
   // eight ranges a request on average, 4 from four; one otherwise, so that an
   // ordinary batch keeps one block per 16 dims.
-  if ((int64_t)batch * 8 <= max_ranges) {
-    dim3 grid(batch, kVDim / kCombDims, 16);
-    plan_combine_kernel<16><<<grid, kHeads, 0, stream>>>(ws, batch, max_ranges,
-                                                         (__nv_bfloat16 *)out, lse);
-  } else if ((int64_t)batch * 4 <= max_ranges) {
-    dim3 grid(batch, kVDim / kCombDims, 4);
-    plan_combine_kernel<4><<<grid, kHeads, 0, stream>>>(ws, batch, max_ranges,
-                                                        (__nv_bfloat16 *)out, lse);
-  } else {
-    dim3 grid(batch, kVDim / kCombDims, 1);
-    plan_combine_kernel<1><<<grid, kHeads, 0, stream>>>(ws, batch, max_ranges,
-                                                        (__nv_bfloat16 *)out, lse);
-  }
-  return cudaGetLastError();
+  const int lanes =
+      (int64_t)batch * 8 <= max_ranges ? 16 : ((int64_t)batch * 4 <= max_ranges ? 4 : 1);
+  // early: a programmatic dependent of the decode, whose CTAs release it once
+  // they have requested their last tile
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(batch, kVDim / kCombDims, lanes);
+  cfg.blockDim = dim3(kHeads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = early ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  __nv_bfloat16 *o = (__nv_bfloat16 *)out;
+  if (lanes == 16)
+    return cudaLaunchKernelEx(&cfg, plan_combine_kernel<16>, ws, batch, max_ranges, o, lse);
+  if (lanes == 4)
+    return cudaLaunchKernelEx(&cfg, plan_combine_kernel<4>, ws, batch, max_ranges, o, lse);
+  return cudaLaunchKernelEx(&cfg, plan_combine_kernel<1>, ws, batch, max_ranges, o, lse);
 }
 
 // Merges the partials of the few-head kernel (decode_tp.cu), stored in bf16
