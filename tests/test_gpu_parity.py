@@ -618,8 +618,10 @@ def test_graph_captured_step_equals_eager(mla, lens):
     """A step captured in a CUDA graph (plan + per-layer fused append and
     decode, on a side stream, as the benchmark runs it) gives the same bits as
     the same calls run eagerly, replay after replay; its outputs match the
-    oracle on sampled requests.  Six requests keep the separate combine;
-    forty merge their splits inside the decode (a cooperative launch)."""
+    oracle on sampled requests.  With six requests the decode is launched
+    normally and its combine as a programmatic dependent of it; with forty
+    the decode is the programmatic dependent (of the previous layer's
+    combine) and the combine is launched normally."""
     w = mi.custom_workload(lens, block_size=64, layers=2, append=True,
                            pool_factor=1.5, name="graph_check")
     bt = mi.make_block_table(mi.rng_for(w.config_id, 0, 1), w.seq_lens, w.block_size,
