@@ -41,6 +41,12 @@
 // of O and write the output (or split partials plus log-sum-exp); warp 4 owns
 // the tensor memory allocation.
 //
+// Launch order.  Launched as a programmatic dependent of the previous kernel
+// (early_launch), a CTA sets up its barriers and tensor memory while that
+// kernel ends and, before griddepcontrol.wait, only asks L2 for its first
+// tile and q; everything it reads or writes comes after the wait.  Each CTA
+// releases its own dependents once it has requested its last tile.
+//
 // FP8 cache (kFp8).  The cache holds one E4M3 byte per element, 576 bytes per
 // token per layer [MLA 的 TP 切分 (10100.com), opening paragraph and section
 // 5.1], with one scale per layer (a code c stands for value(c) * kv_scale).
