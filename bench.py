@@ -176,6 +176,17 @@ def kernel_source_hash():
     return h.hexdigest()
 
 
+def e2e_chunk_bounds(layers, growth=1.6):
+    """Layer boundaries of the e2e step's copy chunks: the input chunks start
+    at one layer and grow by `growth` (the decodes of layers [a, b) wait for
+    the inputs of layers < b); the output chunks mirror them, shrinking
+    towards the last layer.  Both lists run from 0 to `layers`."""
+    b = [0]
+    while b[-1] < layers:
+        b.append(min(layers, max(b[-1] + 1, math.ceil(growth * b[-1]))))
+    return b, [layers - x for x in reversed(b)]
+
+
 def measured_traffic(w):
     """DRAM bytes per decode launch from the committed ncu capture, if it was taken
     on this workload's layer shape with the kernel as it is now; else None."""
@@ -366,14 +377,7 @@ def run_mine(args, w, rank, world, local_rank):
     # chunks mirror them and shrink towards the end, where the last layer's
     # outputs cannot overlap any decode.  (Per-layer edges: +13% on the
     # 61-layer step; uniform chunks of three: +4% against this schedule.)
-    def growing(n):
-        b = [0]
-        while b[-1] < n:
-            b.append(min(n, max(b[-1] + 1, math.ceil(1.6 * b[-1]))))
-        return b
-
-    in_bounds = growing(L)
-    out_bounds = [L - x for x in reversed(in_bounds)]
+    in_bounds, out_bounds = e2e_chunk_bounds(L)
     in_chunks = list(zip(in_bounds[:-1], in_bounds[1:]))
     out_start = {b: a for a, b in zip(out_bounds[:-1], out_bounds[1:])}
 

@@ -61,3 +61,21 @@ def test_single_rank_is_identity():
     import bench
     assert bench.reduce_max(3.5, 1) == 3.5
     assert bench.job_throughput_gbs(1, 2e9, 1000.0) == pytest.approx(2.0)
+
+
+def test_e2e_chunk_bounds():
+    """The e2e step's copy chunks: the input chunks start with layer 0 alone
+    and grow, the output chunks mirror them and end with the last layer
+    alone, both covering every layer once."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.e2e_chunk_bounds(61) == ([0, 1, 2, 4, 7, 12, 20, 32, 52, 61],
+                                          [0, 9, 29, 41, 49, 54, 57, 59, 60, 61])
+    for layers in range(1, 130):
+        ins, outs = bench.e2e_chunk_bounds(layers)
+        for b in (ins, outs):
+            assert b[0] == 0 and b[-1] == layers
+            assert all(x < y for x, y in zip(b, b[1:]))
+        assert ins[1] == 1 and outs[-2] == layers - 1
+        widths = [y - x for x, y in zip(ins, ins[1:])]
+        assert all(w1 <= w2 for w1, w2 in zip(widths[:-2], widths[1:-1]))  # growing, bar the last
